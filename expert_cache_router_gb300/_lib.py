@@ -25,7 +25,8 @@ EXPORTS = [
     "moe_offload_read_prefetch", "moe_offload_read_slot",
     "moe_offload_read_slot_scales", "moe_offload_set_shared_expert", "moe_offload_reset",
     "moe_offload_host_alloc", "moe_offload_host_free", "moe_offload_prefill_times",
-    "moe_offload_device_bytes", "moe_offload_graph_create", "moe_offload_graph_launch",
+    "moe_offload_device_bytes", "moe_offload_get_config", "moe_offload_read_routing",
+    "moe_offload_debug_wait", "moe_offload_graph_create", "moe_offload_graph_launch",
     "moe_offload_graph_launch_host", "moe_offload_graph_times", "moe_offload_graph_kernel_count",
     "moe_offload_graph_destroy", "moe_offload_grouped_ffn_noalloc", "moe_offload_last_error",
     "moe_offload_destroy",
@@ -37,7 +38,7 @@ class Config(ctypes.Structure):
                 ("hidden", ctypes.c_int), ("inter", ctypes.c_int), ("num_slots", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("renormalize", ctypes.c_int),
                 ("max_tokens_graph", ctypes.c_int), ("shared_expert", ctypes.c_int),
-                ("prefetch_n", ctypes.c_int)]
+                ("prefetch_n", ctypes.c_int), ("auto_reserve_bytes", ctypes.c_ulonglong)]
 
 
 class Stats(ctypes.Structure):
@@ -116,6 +117,12 @@ def _declare(L):
     L.moe_offload_prefill_times.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp]
     L.moe_offload_device_bytes.restype = ctypes.c_size_t
     L.moe_offload_device_bytes.argtypes = [_vp]
+    L.moe_offload_get_config.restype = _st
+    L.moe_offload_get_config.argtypes = [_vp, ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_size_t)]
+    L.moe_offload_read_routing.restype = _st
+    L.moe_offload_read_routing.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, _ip]
+    L.moe_offload_debug_wait.restype = _st
+    L.moe_offload_debug_wait.argtypes = [_vp, ctypes.c_longlong, ctypes.c_int]
     L.moe_offload_graph_create.restype = _st
     L.moe_offload_graph_create.argtypes = [_vp, ctypes.c_int, _vp, _vp, ctypes.c_int, ctypes.POINTER(_vp)]
     L.moe_offload_graph_launch.restype = _st

@@ -113,6 +113,9 @@ class MoeOffload:
     dtype      : "bf16" or "fp8" (e4m3 with 128x128 block scales)
     shared_expert: every layer adds an always-resident shared expert (set_shared_expert)
     prefetch_n : router lookahead, experts per layer prefetched from the previous layer's input
+    num_slots  : slots per layer, or 0 for `auto` sizing from the device's free memory less
+                 auto_reserve_bytes (0: the library's 2.5 GiB default); num_slots then holds
+                 the count chosen and auto_free_bytes the free memory the sizing read
     The caller keeps all of them alive until close().
     """
 
@@ -120,12 +123,14 @@ class MoeOffload:
                  num_slots: int, host_w13: Sequence, host_w2: Sequence, router: Sequence,
                  renormalize: bool = True, max_tokens_graph: int = 8, device: int = 0,
                  dtype: str = "bf16", host_s13: Optional[Sequence] = None,
-                 host_s2: Optional[Sequence] = None, shared_expert: bool = False, prefetch_n: int = 0):
+                 host_s2: Optional[Sequence] = None, shared_expert: bool = False, prefetch_n: int = 0,
+                 auto_reserve_bytes: int = 0):
         self._L = C.load()
         code = {"bf16": C.MOE_DTYPE_BF16, "fp8": C.MOE_DTYPE_FP8_E4M3_B128}[dtype]
         self.dtype = dtype
         self.cfg = C.Config(num_layers, num_experts, top_k, hidden, inter, num_slots, code,
-                            int(bool(renormalize)), max_tokens_graph, int(bool(shared_expert)), int(prefetch_n))
+                            int(bool(renormalize)), max_tokens_graph, int(bool(shared_expert)), int(prefetch_n),
+                            int(auto_reserve_bytes))
         self.prefetch_n = int(prefetch_n)
         self.num_layers, self.num_experts, self.top_k = num_layers, num_experts, top_k
         self.hidden, self.inter, self.num_slots = hidden, inter, num_slots
@@ -144,6 +149,11 @@ class MoeOffload:
         if st != C.MOE_OK:
             raise MoeOffloadError(st, self._L.moe_offload_last_error(None).decode())
         self.h = h
+        got = C.Config()
+        free = ctypes.c_size_t()
+        self._check(self._L.moe_offload_get_config(h, ctypes.byref(got), ctypes.byref(free)))
+        self.num_slots = int(got.num_slots)
+        self.auto_free_bytes = int(free.value)
 
     # -- helpers
     def _check(self, st: int) -> None:
@@ -283,6 +293,24 @@ class MoeOffload:
 
     def device_bytes(self) -> int:
         return int(self._L.moe_offload_device_bytes(self.h))
+
+    def read_routing(self):
+        """(ids [T,k], weights [T,k], slot ids [T,k]) of the last decode-path call."""
+        cap = self.max_tokens_graph * self.top_k
+        ids = np.zeros(cap, np.int32)
+        w = np.zeros(cap, np.float32)
+        sl = np.zeros(cap, np.int32)
+        n = ctypes.c_int()
+        self._check(self._L.moe_offload_read_routing(self.h, ids.ctypes.data, w.ctypes.data, sl.ctypes.data, cap,
+                                                     ctypes.byref(n)))
+        m = n.value
+        k = self.top_k
+        return ids[:m].reshape(-1, k), w[:m].reshape(-1, k), sl[:m].reshape(-1, k)
+
+    def debug_wait(self, limit_ns: int = 0, stall: bool = False) -> None:
+        """Bound of the decode step's early-down waits (0: default) and the debug stall
+        that makes the first group's wait of every down warp run out."""
+        self._check(self._L.moe_offload_debug_wait(self.h, int(limit_ns), int(bool(stall))))
 
     def prefill_times(self) -> dict:
         """Phase times (ms) of the last prefill call: route, copy, gemm, combine, staged."""

@@ -51,6 +51,12 @@ struct moe_offload {
   int audit_each = 0;  // env MOE_OFFLOAD_AUDIT=1: audit a layer's table after every update of it
   int early_down = 1;  // env MOE_OFFLOAD_EARLY_DOWN=0: the down launch waits for the whole gate/up grid
   uint32_t* ffn_sync = nullptr;  // [kFfnSyncWords] counters of the early-down hand-off
+  int last_tk = 0;               // T * k of the last decode-path call (ids_buf, w_buf, slot_buf)
+  // Bound of the early-down waits, and the debug stall that plants a target no
+  // counter reaches (moe_offload_debug_wait).
+  unsigned long long wait_ns = kDefaultWaitNs;
+  int stall = 0;
+  size_t auto_free = 0;          // num_slots = 0 at create: free device bytes the sizing saw
 
   // Eager decode profile (env MOE_OFFLOAD_PROFILE=1): events before the head, after the head,
   // after gate/up and after down of every decode_layer call outside stream capture; folded into
@@ -86,6 +92,7 @@ struct moe_offload {
 namespace {
 
 thread_local std::string g_create_error;
+constexpr size_t kAutoReserveBytes = (size_t)5 << 29;  // 2.5 GiB, the page's default reserve
 
 moe_status_t fail(moe_offload* h, moe_status_t st, const char* fmt, ...) {
   char buf[512];
@@ -275,6 +282,8 @@ FfnArgs ffn_args(moe_offload* h, int layer, const void* x, const int32_t* slot_i
   a.fmt = h->fmt;
   a.shared = h->cfg.shared_expert ? 1 : 0;
   a.pair_src = h->tab[layer].pair_src;
+  a.wait_ns = h->wait_ns;
+  a.stall = h->stall;
   return a;
 }
 
@@ -490,7 +499,8 @@ moe_status_t moe_offload_create(const moe_offload_config_t* cfg, int device, voi
   const moe_offload_config_t c = *cfg;
   if (c.num_layers < 1 || c.num_experts < 1 || c.num_experts > 1024 || c.top_k < 1 || c.top_k > 16 ||
       c.top_k > c.num_experts || c.hidden < 256 || c.hidden % 256 != 0 || c.hidden > 8192 ||
-      c.inter < 64 || c.inter % 64 != 0 || c.num_slots < c.top_k || c.num_slots > c.num_experts ||
+      c.inter < 64 || c.inter % 64 != 0 ||
+      (c.num_slots != 0 && (c.num_slots < c.top_k || c.num_slots > c.num_experts)) ||
       c.max_tokens_graph < 1 || c.max_tokens_graph > 64 || c.max_tokens_graph * c.top_k > 1024)
     return fail(nullptr, MOE_ERR_INVALID,
                 "invalid configuration (L=%d E=%d k=%d H=%d I=%d S=%d Tmax=%d)", c.num_layers,
@@ -500,8 +510,9 @@ moe_status_t moe_offload_create(const moe_offload_config_t* cfg, int device, voi
   const bool fp8 = c.dtype == MOE_DTYPE_FP8_E4M3_B128;
   if (c.shared_expert != 0 && c.shared_expert != 1)
     return fail(nullptr, MOE_ERR_INVALID, "shared_expert must be 0 or 1");
-  if (c.prefetch_n < 0 || c.prefetch_n > c.num_slots)
-    return fail(nullptr, MOE_ERR_INVALID, "prefetch_n=%d outside [0, num_slots=%d]", c.prefetch_n, c.num_slots);
+  const int s_bound = c.num_slots ? c.num_slots : c.num_experts;  // auto: checked again once S is known
+  if (c.prefetch_n < 0 || c.prefetch_n > s_bound)
+    return fail(nullptr, MOE_ERR_INVALID, "prefetch_n=%d outside [0, num_slots=%d]", c.prefetch_n, s_bound);
   if (c.max_tokens_graph * (c.top_k + c.shared_expert) > 1024)
     return fail(nullptr, MOE_ERR_INVALID, "max_tokens_graph * (top_k + shared_expert) above 1024");
   if (fp8) {
@@ -525,7 +536,7 @@ moe_status_t moe_offload_create(const moe_offload_config_t* cfg, int device, voi
   if (!h) return fail(nullptr, MOE_ERR_OOM, "out of host memory");
   h->cfg = c;
   h->device = device;
-  const int L = c.num_layers, E = c.num_experts, S = c.num_slots, H = c.hidden, I = c.inter;
+  const int L = c.num_layers, E = c.num_experts, H = c.hidden, I = c.inter;
   const int Tmax = c.max_tokens_graph, k = c.top_k;
   h->w13_elems = (size_t)2 * I * H;
   h->w2_elems = (size_t)H * I;
@@ -587,8 +598,6 @@ moe_status_t moe_offload_create(const moe_offload_config_t* cfg, int device, voi
     if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaHostGetDevicePointer"));
     h->lw[l].host_w13 = static_cast<const uint8_t*>(d13);
     h->lw[l].host_w2 = static_cast<const uint8_t*>(d2);
-    if ((st = dev_alloc(h, &h->lw[l].slot_w13, (size_t)S * h->e13_bytes)) != MOE_OK) return bail(st);
-    if ((st = dev_alloc(h, &h->lw[l].slot_w2, (size_t)S * h->e2_bytes)) != MOE_OK) return bail(st);
     if (fp8) {
       void* q13 = nullptr;
       void* q2 = nullptr;
@@ -597,10 +606,81 @@ moe_status_t moe_offload_create(const moe_offload_config_t* cfg, int device, voi
       if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaHostGetDevicePointer (scales)"));
       h->lw[l].host_s13 = static_cast<const float*>(q13);
       h->lw[l].host_s2 = static_cast<const float*>(q2);
+    }
+    h->router[l] = static_cast<const uint16_t*>(dev_router[l]);
+  }
+
+  // Decode scratch.
+  const size_t tk = (size_t)Tmax * k;
+  if ((st = dev_alloc(h, &h->ids_buf, sizeof(int32_t) * tk)) != MOE_OK ||
+      (st = dev_alloc(h, &h->w_buf, sizeof(float) * tk)) != MOE_OK ||
+      (st = dev_alloc(h, &h->slot_buf, sizeof(int32_t) * tk)) != MOE_OK ||
+      (st = dev_alloc(h, &h->logits, sizeof(float) * (size_t)Tmax * E)) != MOE_OK ||
+      (st = dev_alloc(h, &h->hbuf, sizeof(float) * (tk + (size_t)Tmax * c.shared_expert) * I)) != MOE_OK ||
+      (st = dev_alloc(h, &h->route_done, sizeof(unsigned) * L)) != MOE_OK ||
+      (st = dev_alloc(h, &h->status, sizeof(uint32_t))) != MOE_OK ||
+      (st = dev_alloc(h, &h->ffn_sync, sizeof(uint32_t) * kFfnSyncWords)) != MOE_OK)
+    return bail(st);
+  {
+    cudaError_t e = cudaMemset(h->route_done, 0, sizeof(unsigned) * L);
+    if (e == cudaSuccess) e = cudaMemset(h->ffn_sync, 0, sizeof(uint32_t) * kFfnSyncWords);
+    if (e == cudaSuccess) e = cudaMemset(h->ids_buf, 0, sizeof(int32_t) * tk);
+    if (e == cudaSuccess) e = cudaMemset(h->w_buf, 0, sizeof(float) * tk);
+    if (e == cudaSuccess) e = cudaMemset(h->slot_buf, 0, sizeof(int32_t) * tk);
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaMemset"));
+  }
+  h->pf_pending.assign(L, 0);
+  if (c.prefetch_n > 0) {
+    if ((st = dev_alloc(h, &h->pred_logits, sizeof(float) * (size_t)Tmax * E)) != MOE_OK ||
+        (st = dev_alloc(h, &h->pred_ids, sizeof(int32_t) * tk)) != MOE_OK ||
+        (st = dev_alloc(h, &h->pred_w, sizeof(float) * tk)) != MOE_OK ||
+        (st = dev_alloc(h, &h->pred_done, sizeof(unsigned))) != MOE_OK)
+      return bail(st);
+    cudaError_t e = cudaMemset(h->pred_done, 0, sizeof(unsigned));
+    int lo = 0, hi = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->pf_stream, cudaStreamNonBlocking, hi);
+    h->pf_ready.assign(L, nullptr);
+    h->pf_done.assign(L, nullptr);
+    for (int l = 0; l < L && e == cudaSuccess; ++l) {
+      e = cudaEventCreateWithFlags(&h->pf_ready[l], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->pf_done[l], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "prefetch stream and events"));
+  }
+  {
+    cudaError_t e = prefill_create(&h->prefill, E, c.shared_expert, H, I, h->w13_elems, h->w2_elems, &h->dev_bytes);
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "prefill buffers"));
+  }
+
+  // `auto` slot count: every other allocation is made; the layers' slots grow
+  // evenly into what is free, less the reserve ("MoE expert offload" page,
+  // Options table: auto sizing after loading, XINFER_MOE_OFFLOAD_RESERVE_GB).
+  if (c.num_slots == 0) {
+    size_t free_b = 0, total_b = 0;
+    cudaError_t e = cudaMemGetInfo(&free_b, &total_b);
+    if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaMemGetInfo"));
+    const size_t reserve = c.auto_reserve_bytes ? (size_t)c.auto_reserve_bytes : kAutoReserveBytes;
+    const int s_auto = moe_offload_slots_auto(free_b, reserve, L, E, k, (size_t)slot_bytes(h));
+    h->auto_free = free_b;
+    if (s_auto < 0)
+      return bail(fail(h, MOE_ERR_OOM, "auto slots: %zu free bytes less a %zu-byte reserve hold fewer than "
+                       "top_k=%d slots per layer of %llu bytes x %d layers", free_b, reserve, k,
+                       slot_bytes(h), L));
+    if (c.prefetch_n > s_auto)
+      return bail(fail(h, MOE_ERR_INVALID, "prefetch_n=%d above the %d auto slots", c.prefetch_n, s_auto));
+    h->cfg.num_slots = s_auto;
+  }
+  const int S = h->cfg.num_slots;
+
+  // Slot tensors.
+  for (int l = 0; l < L; ++l) {
+    if ((st = dev_alloc(h, &h->lw[l].slot_w13, (size_t)S * h->e13_bytes)) != MOE_OK) return bail(st);
+    if ((st = dev_alloc(h, &h->lw[l].slot_w2, (size_t)S * h->e2_bytes)) != MOE_OK) return bail(st);
+    if (fp8) {
       if ((st = dev_alloc(h, &h->lw[l].slot_s13, sizeof(float) * S * h->f13)) != MOE_OK) return bail(st);
       if ((st = dev_alloc(h, &h->lw[l].slot_s2, sizeof(float) * S * h->f2)) != MOE_OK) return bail(st);
     }
-    h->router[l] = static_cast<const uint16_t*>(dev_router[l]);
   }
 
   // Slot tables: one block, a 256-byte-aligned record per layer.
@@ -628,47 +708,7 @@ moe_status_t moe_offload_create(const moe_offload_config_t* cfg, int device, voi
     t.pair_src = reinterpret_cast<int32_t*>(p); p += up(sizeof(int32_t) * kMaxCallPairs);
     t.stats = reinterpret_cast<unsigned long long*>(p);
   }
-
-  // Decode scratch.
-  const size_t tk = (size_t)Tmax * k;
-  if ((st = dev_alloc(h, &h->ids_buf, sizeof(int32_t) * tk)) != MOE_OK ||
-      (st = dev_alloc(h, &h->w_buf, sizeof(float) * tk)) != MOE_OK ||
-      (st = dev_alloc(h, &h->slot_buf, sizeof(int32_t) * tk)) != MOE_OK ||
-      (st = dev_alloc(h, &h->logits, sizeof(float) * (size_t)Tmax * E)) != MOE_OK ||
-      (st = dev_alloc(h, &h->hbuf, sizeof(float) * (tk + (size_t)Tmax * c.shared_expert) * I)) != MOE_OK ||
-      (st = dev_alloc(h, &h->route_done, sizeof(unsigned) * L)) != MOE_OK ||
-      (st = dev_alloc(h, &h->status, sizeof(uint32_t))) != MOE_OK ||
-      (st = dev_alloc(h, &h->ffn_sync, sizeof(uint32_t) * kFfnSyncWords)) != MOE_OK)
-    return bail(st);
-  {
-    cudaError_t e = cudaMemset(h->route_done, 0, sizeof(unsigned) * L);
-    if (e == cudaSuccess) e = cudaMemset(h->ffn_sync, 0, sizeof(uint32_t) * kFfnSyncWords);
-    if (e != cudaSuccess) return bail(cuda_fail(h, e, "cudaMemset"));
-  }
-  h->pf_pending.assign(L, 0);
-  if (c.prefetch_n > 0) {
-    if ((st = dev_alloc(h, &h->pred_logits, sizeof(float) * (size_t)Tmax * E)) != MOE_OK ||
-        (st = dev_alloc(h, &h->pred_ids, sizeof(int32_t) * tk)) != MOE_OK ||
-        (st = dev_alloc(h, &h->pred_w, sizeof(float) * tk)) != MOE_OK ||
-        (st = dev_alloc(h, &h->pred_done, sizeof(unsigned))) != MOE_OK)
-      return bail(st);
-    cudaError_t e = cudaMemset(h->pred_done, 0, sizeof(unsigned));
-    int lo = 0, hi = 0;
-    if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
-    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h->pf_stream, cudaStreamNonBlocking, hi);
-    h->pf_ready.assign(L, nullptr);
-    h->pf_done.assign(L, nullptr);
-    for (int l = 0; l < L && e == cudaSuccess; ++l) {
-      e = cudaEventCreateWithFlags(&h->pf_ready[l], cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->pf_done[l], cudaEventDisableTiming);
-    }
-    if (e != cudaSuccess) return bail(cuda_fail(h, e, "prefetch stream and events"));
-  }
   if ((st = init_tables(h)) != MOE_OK) return bail(st);
-  {
-    cudaError_t e = prefill_create(&h->prefill, E, c.shared_expert, H, I, h->w13_elems, h->w2_elems, &h->dev_bytes);
-    if (e != cudaSuccess) return bail(cuda_fail(h, e, "prefill buffers"));
-  }
   // First GPU read of the host store: on GB300 the first pass of GPU reads over
   // host pages the CPU had just written ran well below the link rate (a
   // 256-token decode pass at 189 tok/s where later passes ran at 262), so the
@@ -770,6 +810,7 @@ moe_status_t moe_offload_decode_layer(moe_offload_t h, int layer, const void* x,
   if ((st = set_device(h)) != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (T <= h->cfg.max_tokens_graph) {
+    h->last_tk = T * h->cfg.top_k;
     if (h->profile && !capturing(s)) return profiled_decode(h, layer, x, T, out, s);
     if ((st = do_decode_head(h, layer, x, T, s)) != MOE_OK) return st;
     return do_decode_ffn(h, layer, x, T, out, s);
@@ -1134,6 +1175,37 @@ moe_status_t moe_offload_prefill_times(moe_offload_t h, float* route_ms, float* 
 
 size_t moe_offload_device_bytes(moe_offload_t h) { return h ? h->dev_bytes : 0; }
 
+moe_status_t moe_offload_get_config(moe_offload_t h, moe_offload_config_t* cfg, size_t* auto_free_bytes) {
+  if (!h) return MOE_ERR_INVALID;
+  if (cfg) *cfg = h->cfg;
+  if (auto_free_bytes) *auto_free_bytes = h->auto_free;
+  return MOE_OK;
+}
+
+moe_status_t moe_offload_read_routing(moe_offload_t h, int32_t* ids, float* w, int32_t* slot_ids, int cap,
+                                      int* n_pairs) {
+  if (!h) return MOE_ERR_INVALID;
+  if (cap < 0) return fail(h, MOE_ERR_INVALID, "cap < 0");
+  moe_status_t st = set_device(h);
+  if (st != MOE_OK) return st;
+  CK(h, cudaDeviceSynchronize());
+  if (n_pairs) *n_pairs = h->last_tk;
+  const int n = std::min(cap, h->last_tk);
+  if (n > 0 && ids) CK(h, cudaMemcpy(ids, h->ids_buf, sizeof(int32_t) * n, cudaMemcpyDeviceToHost));
+  if (n > 0 && w) CK(h, cudaMemcpy(w, h->w_buf, sizeof(float) * n, cudaMemcpyDeviceToHost));
+  if (n > 0 && slot_ids) CK(h, cudaMemcpy(slot_ids, h->slot_buf, sizeof(int32_t) * n, cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+moe_status_t moe_offload_debug_wait(moe_offload_t h, long long limit_ns, int stall) {
+  if (!h) return MOE_ERR_INVALID;
+  if (limit_ns < 0 || (stall != 0 && stall != 1))
+    return fail(h, MOE_ERR_INVALID, "debug_wait: limit_ns=%lld stall=%d", limit_ns, stall);
+  h->wait_ns = limit_ns ? (unsigned long long)limit_ns : kDefaultWaitNs;
+  h->stall = stall;
+  return MOE_OK;
+}
+
 const char* moe_offload_last_error(moe_offload_t h) {
   return h ? h->err.c_str() : g_create_error.c_str();
 }
@@ -1312,6 +1384,7 @@ moe_status_t moe_offload_graph_launch(moe_offload_graph_t g, moe_stream_t stream
   moe_status_t st = set_device(h);
   if (st != MOE_OK) return st;
   CK(h, cudaGraphLaunch(g->exec, reinterpret_cast<cudaStream_t>(stream)));
+  h->last_tk = g->T * h->cfg.top_k;
   return MOE_OK;
 }
 
@@ -1325,6 +1398,7 @@ moe_status_t moe_offload_graph_launch_host(moe_offload_graph_t g, const void* x_
   const size_t bytes = (size_t)h->cfg.num_layers * g->T * h->cfg.hidden * 2;
   CK(h, cudaMemcpyAsync(const_cast<uint16_t*>(g->x), x_host, bytes, cudaMemcpyHostToDevice, s));
   CK(h, cudaGraphLaunch(g->exec, s));
+  h->last_tk = g->T * h->cfg.top_k;
   CK(h, cudaMemcpyAsync(out_host, g->out, bytes, cudaMemcpyDeviceToHost, s));
   CK(h, cudaStreamSynchronize(s));
   return MOE_OK;

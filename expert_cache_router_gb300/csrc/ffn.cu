@@ -54,7 +54,6 @@ constexpr int kCopyCols = 4;  // copy-through: extra grid columns of W2 copy wor
 constexpr int kSyncCopy = kSyncCopyLine * kSyncLine;  // early down: W2-copy CTAs done
 constexpr int kSyncDone = kSyncDoneLine * kSyncLine;  // early down: down CTAs done
 static_assert(kSyncColumns >= kMaxPairs + 1, "early-down counters");
-constexpr unsigned long long kWaitNs = 2000000000ull;  // bound of one early-down wait
 
 template <int FMT>
 struct Fmt;
@@ -491,6 +490,7 @@ ffn_down_combine_kernel(FfnArgs a) {
   }
   __syncthreads();
   const uint32_t gate_ctas = (uint32_t)((I + kGateRowsPerCta - 1) / kGateRowsPerCta);
+  const unsigned long long wait_ns = a.wait_ns ? a.wait_ns : kDefaultWaitNs;
   const uint32_t copy_ctas = a.copy_through ? (uint32_t)kCopyCols * gate_ctas : 0u;
   const int r0 = blockIdx.x * kDownRowsPerCta;
   const int ib = I >> 7;
@@ -530,9 +530,11 @@ ffn_down_combine_kernel(FfnArgs a) {
     }
     if (!w2 && lane == 0) atomicOr(a.status, kDevBadSlotId);
     if (a.sync) {
-      if (lane == 0 && wait_at_least(a.sync + (d < s_groups ? p0 : Tk) * kSyncLine, gate_ctas, a.status, kWaitNs) &&
+      // (a.stall: the first group's target is one more CTA than its column has, so it runs out)
+      const uint32_t target = gate_ctas + (a.stall && d == 0 ? 1u : 0u);
+      if (lane == 0 && wait_at_least(a.sync + (d < s_groups ? p0 : Tk) * kSyncLine, target, a.status, wait_ns) &&
           filled)
-        wait_at_least(a.sync + kSyncCopy, copy_ctas, a.status, kWaitNs);
+        wait_at_least(a.sync + kSyncCopy, copy_ctas, a.status, wait_ns);
       __syncwarp();
       if (d + kWarps >= ngroups) waits_done();
     }
@@ -616,7 +618,7 @@ ffn_down_combine_kernel(FfnArgs a) {
   }
   if (a.sync && s_last) {  // every down CTA is past its waits: let the gate/up grid complete, reset
     if (threadIdx.x == 0) {
-      if (copy_ctas) wait_at_least(a.sync + kSyncCopy, copy_ctas, a.status, kWaitNs);
+      if (copy_ctas) wait_at_least(a.sync + kSyncCopy, copy_ctas, a.status, wait_ns);
       pdl_wait();
     }
     __syncthreads();

@@ -126,6 +126,9 @@ struct FfnArgs {
   int shared;               // 1: add the shared expert (lw.sh_*) to every token, weight 1, after the k ranks
   uint32_t* sync;           // early down: [kFfnSyncWords] zeroed counters, or nullptr (down waits for
                             // the whole gate/up grid)
+  unsigned long long wait_ns;  // bound of one early-down wait (0: kDefaultWaitNs)
+  int stall;                // debug: the first group's wait of every down warp targets one CTA more
+                            // than its column has, so it runs out (tests of the bounded wait)
 };
 // Counters of the early-down hand-off of a decode step, one 128-byte line each
 // (so that pollers of different counters do not queue on one L2 line): line
@@ -138,6 +141,7 @@ constexpr int kSyncCopyLine = kSyncColumns;
 constexpr int kSyncDoneLine = kSyncColumns + 1;
 constexpr int kFfnSyncWords = (kSyncDoneLine + 1) * kSyncLine;
 constexpr int kDownRowsPerCta = 8;  // output rows per CTA of the down + combine launch
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // bound of one early-down wait
 cudaError_t launch_grouped_ffn(const FfnArgs& a, cudaStream_t st);
 // Opt the down launch into the dynamic shared memory of its largest calls (T*k up to 1024 pairs);
 // once per device, before the first launch with more than 64 pairs.

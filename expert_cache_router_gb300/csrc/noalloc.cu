@@ -11,14 +11,17 @@
 //
 // The array is a module-scope __device__ variable: every GPU that loads the
 // library holds it until the process exits. In host code its name is only a
-// host-side stand-in, so the device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and that address is what the
-// kernels receive. All calls on a device share the array, which keeps the last
-// call's contents; calls that overlap on the GPU (two streams, or two threads
-// without ordering) race on it.
+// host-side stand-in, so each call looks the device address up with
+// cudaGetSymbolAddress in the calling thread's current context and passes that
+// address to the kernels. A symbol's address belongs to a context, not to a
+// device: a runtime that calls this under its own context, or after a device
+// reset, gets the address valid there (the lookup is cheap once the module is
+// loaded in that context; with lazy loading the first call loads it and places
+// the array, which is why callers make that first call at start-up). All calls
+// on a device share the array, which keeps the last call's contents; calls that
+// overlap on the GPU (two streams, or two threads without ordering) race on it.
 #include <cuda_runtime.h>
 
-#include <mutex>
 #include <string>
 
 #include "../../include/moe_offload.h"
@@ -29,7 +32,10 @@ namespace {
 
 constexpr int kNoAllocMaxPairs = 64;                  // T * top_k
 constexpr size_t kNoAllocFloats = (size_t)1 << 20;    // h rows: T*k*I floats (4 MiB)
-// layout: [h floats | counts | status], each part 256-byte aligned
+// layout: [h floats | counts | status], each part 256-byte aligned. With no
+// copy-through and no host sources (pair_src = nullptr) the FFN kernels never
+// read the count area; it only gives counts/miss_expert a valid address. The
+// status word collects device-detected errors when the caller passes none.
 constexpr size_t kOffCounts = kNoAllocFloats * sizeof(float);
 constexpr size_t kOffStatus = kOffCounts + 256;
 constexpr size_t kNoAllocBytes = kOffStatus + 256;
@@ -37,29 +43,17 @@ static_assert(kNumCounts * sizeof(int32_t) <= 256, "count area");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-unsigned char* g_scratch_dev[kMaxDevices] = {};
-
 moe_status_t noalloc_fail(moe_status_t st, const std::string& msg) {
   set_handleless_error(msg.c_str());  // read back with moe_offload_last_error(NULL)
   return st;
 }
 
-// Device address of the scratch array on the current device (looked up once per device).
-cudaError_t scratch_on_current_device(unsigned char** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+// Device address of the scratch array in the current context.
+cudaError_t scratch_in_current_context(unsigned char** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_dev[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_dev[dev] = static_cast<unsigned char*>(p);
-  }
-  *out = g_scratch_dev[dev];
+  *out = static_cast<unsigned char*>(p);
   return cudaSuccess;
 }
 
@@ -97,16 +91,11 @@ extern "C" moe_status_t moe_offload_grouped_ffn_noalloc(const void* w13, const v
                                              " floats exceed the fixed scratch of " +
                                              std::to_string(kNoAllocFloats) + " floats (4 MiB)");
   unsigned char* base = nullptr;
-  cudaError_t e = scratch_on_current_device(&base);
+  cudaError_t e = scratch_in_current_context(&base);
   if (e != cudaSuccess)
     return noalloc_fail(MOE_ERR_CUDA, std::string("grouped_ffn_noalloc: cudaGetSymbolAddress: ") +
                                           cudaGetErrorString(e));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // The counts must start at zero (no spills: every id names an expert array row).
-  e = cudaMemsetAsync(base + kOffCounts, 0, kOffStatus + 256 - kOffCounts, st);
-  if (e != cudaSuccess)
-    return noalloc_fail(MOE_ERR_CUDA, std::string("grouped_ffn_noalloc: cudaMemsetAsync: ") +
-                                          cudaGetErrorString(e));
   float* fl = reinterpret_cast<float*>(base);
   FfnArgs a{};
   a.lw.host_w13 = nullptr;

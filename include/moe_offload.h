@@ -81,7 +81,11 @@ typedef struct {
   int top_k;            /* k, 1..16 and <= E */
   int hidden;           /* H, multiple of 256, <= 8192 */
   int inter;            /* I (expert intermediate size), multiple of 64 */
-  int num_slots;        /* S per layer, top_k <= S <= E (else MOE_ERR_INVALID) */
+  int num_slots;        /* S per layer, top_k <= S <= E (else MOE_ERR_INVALID); 0 = auto:
+                           after its other allocations create reads the device's free memory
+                           and takes S = moe_offload_slots_auto(free, auto_reserve_bytes, L, E,
+                           top_k, bytes of one slot) (MOE_ERR_OOM when fewer than top_k fit);
+                           moe_offload_get_config returns the S chosen */
   int dtype;            /* MOE_DTYPE_BF16, or MOE_DTYPE_FP8_E4M3_B128 (H and I multiples of 128) */
   int renormalize;      /* 1: weights = softmax over the k chosen logits;
                            0: weights = softmax over all E, taken at the k chosen */
@@ -93,6 +97,9 @@ typedef struct {
   int prefetch_n;       /* router lookahead: 0 = off, else 1..num_slots experts per layer
                            predicted from the previous layer's input and prefetched
                            (see moe_offload_prefetch) */
+  unsigned long long auto_reserve_bytes; /* num_slots = 0 only: device memory left free after the
+                           slots ("MoE expert offload" page, Options table:
+                           XINFER_MOE_OFFLOAD_RESERVE_GB, 2.5 by default); 0 = 2.5 GiB */
 } moe_offload_config_t;
 
 typedef struct {
@@ -290,8 +297,6 @@ moe_status_t moe_offload_read_misses(moe_offload_t h, int layer, int32_t* miss_e
                                      int32_t* miss_slot, int cap, int* miss_count,
                                      int* spill_count);
 
-/* Copy the contents of slot `slot` of `layer` to host buffers (synchronises):
- * w13_out receives 2*I*H bf16 values, w2_out H*I. Either may be NULL. */
 /* Router lookahead and prefetch install into `layer` (FreeToken issue #677,
  * "Proposal": the next layer's router run on the current layer's input predicts
  * the next layer's experts, which are copied while the current layer computes).
@@ -345,6 +350,9 @@ moe_status_t moe_offload_set_placement(moe_offload_t h, int layer, const int32_t
 moe_status_t moe_offload_read_prefetch(moe_offload_t h, int layer, int32_t* cand, int* n_cand, int32_t* experts,
                                        int32_t* slots, int* n_installed, int cap);
 
+/* Copy the contents of slot `slot` of `layer` to host buffers (synchronises):
+ * w13_out receives 2*I*H weights, w2_out H*I (bf16, or e4m3 bytes for FP8
+ * handles). Either may be NULL. For tests. */
 moe_status_t moe_offload_read_slot(moe_offload_t h, int layer, int slot, void* w13_out, void* w2_out);
 
 /* Copies the fp32 block scales slot `slot` of `layer` holds into s13_out
@@ -392,6 +400,34 @@ moe_status_t moe_offload_prefill_times(moe_offload_t h, float* route_ms, float* 
 
 /* Bytes of device memory the handle holds. */
 size_t moe_offload_device_bytes(moe_offload_t h);
+
+/* The handle's configuration as create fixed it (num_slots holds the S an
+ * `auto` create chose) and, for num_slots = 0 at create, the free device bytes
+ * the sizing read (else 0). Either pointer may be NULL. Host only. */
+moe_status_t moe_offload_get_config(moe_offload_t h, moe_offload_config_t* cfg, size_t* auto_free_bytes);
+
+/* Routing of the last decode-path call (decode_layer with T <= max_tokens_graph,
+ * or a decode-graph replay, whose last layer it is): routed expert ids [T,k],
+ * their weights [T,k] and the slot ids (or spill markers) the slot update wrote,
+ * in the handle's own buffers ("MoE expert offload" page, "How it works": ids
+ * rewritten to slot ids). *n_pairs = T*k of that call (0 before any); at most
+ * `cap` entries of each array are written; any pointer may be NULL.
+ * Synchronises the device. For tests that replay the GPU's own routed ids
+ * through the LRU simulator. */
+moe_status_t moe_offload_read_routing(moe_offload_t h, int32_t* ids, float* w, int32_t* slot_ids, int cap,
+                                      int* n_pairs);
+
+/* Bounded waits, for tests that make one run out (no counterpart on the pages).
+ * In a decode step the down launch waits per expert group, on counters the
+ * gate/up CTAs raise, for at most limit_ns (0 = the default, 2 s) per wait;
+ * when a wait runs out the kernel sets MOE_DEV_TIMEOUT, computes on, and every
+ * later wait of the handle returns at once until moe_offload_reset, so outputs
+ * are invalid while the bit is set. stall = 1 makes the first group's wait of
+ * every down warp target one gate/up CTA more than its column has: it runs out
+ * after limit_ns on each later decode step; stall = 0 removes that. Host only;
+ * applies to launches enqueued after the call (decode graphs keep the values
+ * they were captured with). */
+moe_status_t moe_offload_debug_wait(moe_offload_t h, long long limit_ns, int stall);
 
 /* ---- Decode step as one CUDA graph -------------------------------------
  * A decode step of the whole stack (moe_offload_decode_layer for layers
@@ -453,14 +489,18 @@ void moe_offload_graph_destroy(moe_offload_graph_t g);
  * H a multiple of 256 up to 8192, I a multiple of 64; weights, x and out
  * 16-byte aligned. Larger sizes return MOE_ERR_INVALID with the reason in
  * moe_offload_last_error(NULL); nothing is launched then.
- * It runs on the calling thread's current device. The scratch is a
- * file-scope __device__ array of about 4 MiB that every GPU loading the
- * library holds until the process exits; the first call on a device looks
- * its address up (cudaGetSymbolAddress), so make that first call before any
- * stream capture on that device. It allocates nothing: no cudaMalloc, no
- * cudaFree, no allocating library routine. Every call on a device shares the
- * array and it keeps the last call's contents (the counts that must start at
- * zero are cleared by each call); calls that overlap on the GPU race on it. */
+ * It runs on the calling thread's current device and context. The scratch is
+ * a file-scope __device__ array of about 4 MiB that every GPU loading the
+ * library holds until the process exits. Each call looks up the array's
+ * address in the current context (cudaGetSymbolAddress), so a context that was
+ * reset or replaced gets the address that is valid in it. With lazy module
+ * loading (the CUDA default) the first call in a context loads the library's
+ * device code there and places the array: make that first call at start-up,
+ * before any stream capture, so that later calls allocate nothing. No call
+ * allocates: no cudaMalloc, no cudaFree, no allocating library routine. Every
+ * call on a device shares the array and it keeps the last call's contents
+ * (nothing read from it needs to start at zero: each call writes every
+ * intermediate row it reads); calls that overlap on the GPU race on it. */
 moe_status_t moe_offload_grouped_ffn_noalloc(const void* w13, const void* w2, int num_experts,
                                              int hidden, int inter, const void* x, const int32_t* ids,
                                              const float* w, int T, int top_k, void* out,

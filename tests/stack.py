@@ -27,7 +27,7 @@ class Stack:
                                 for l in range(self.cfg.num_layers)]
         return self._router_dev
 
-    def handle(self, torch, dev, num_slots=None, max_tokens_graph=8, prefetch_n=0):
+    def handle(self, torch, dev, num_slots=None, max_tokens_graph=8, prefetch_n=0, auto_reserve_bytes=0):
         from expert_cache_router_gb300 import MoeOffload
         c = self.cfg
         return MoeOffload(num_layers=c.num_layers, num_experts=c.num_experts, top_k=c.top_k,
@@ -36,7 +36,8 @@ class Stack:
                           host_w13=[self.w13[l] for l in range(c.num_layers)],
                           host_w2=[self.w2[l] for l in range(c.num_layers)],
                           router=self.router_dev(torch, dev), renormalize=c.renormalize,
-                          max_tokens_graph=max_tokens_graph, prefetch_n=prefetch_n)
+                          max_tokens_graph=max_tokens_graph, prefetch_n=prefetch_n,
+                          auto_reserve_bytes=auto_reserve_bytes)
 
 
 def rel_l2(got, want) -> float:

@@ -101,7 +101,25 @@ def test_null_handle_calls_are_rejected(lib):
     assert lib.moe_offload_profile_read(None, -1, None, None, None, None, 0) == C.MOE_ERR_INVALID
     assert lib.moe_offload_debug_write_table(None, 0, 0, 0, 0) == C.MOE_ERR_INVALID
     assert lib.moe_offload_audit(None, 0, None) == C.MOE_ERR_INVALID
+    assert lib.moe_offload_get_config(None, None, None) == C.MOE_ERR_INVALID
+    assert lib.moe_offload_read_routing(None, None, None, None, 0, None) == C.MOE_ERR_INVALID
+    assert lib.moe_offload_debug_wait(None, 0, 0) == C.MOE_ERR_INVALID
     lib.moe_offload_destroy(None)
+
+
+def test_auto_slot_config_is_checked_without_gpu(lib):
+    """num_slots = 0 asks for auto sizing; the host checks that need no device still apply."""
+    from expert_cache_router_gb300 import _lib as C
+    buf = np.zeros(64, np.uint16)
+    arr = ctypes.c_void_p * 1
+    p = arr(buf.ctypes.data)
+    h = ctypes.c_void_p()
+    cfg = C.Config(1, 8, 2, 256, 512, 0, 0, 1, 8, 0, 9, 0)    # auto, prefetch_n above E
+    assert lib.moe_offload_create(ctypes.byref(cfg), 0, p, p, None, None, p, ctypes.byref(h)) == C.MOE_ERR_INVALID
+    assert b"prefetch_n" in lib.moe_offload_last_error(None)
+    cfg = C.Config(1, 8, 2, 256, 512, -1, 0, 1, 8, 0, 0, 0)   # negative slot count
+    assert lib.moe_offload_create(ctypes.byref(cfg), 0, p, p, None, None, p, ctypes.byref(h)) == C.MOE_ERR_INVALID
+    assert not h.value
 
 
 def test_slots_auto_matches_oracle(lib):

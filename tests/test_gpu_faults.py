@@ -168,3 +168,62 @@ def test_injected_allocation_failures_release_everything(dev, tiny, monkeypatch)
         assert h.get_stats()["device_status"] == 0
     finally:
         h.close()
+
+
+def test_bounded_early_down_wait_runs_out_and_reset_recovers(dev, tiny):
+    """A bounded device wait made to run out, with no fault: the down launch of a
+    decode step waits per expert group on counters the gate/up CTAs raise. With
+    a 1 ms bound and the debug stall (the first group's target is one CTA more
+    than its column has) the wait runs out: the call returns at once rather than
+    after the 2 s default, the status word carries MOE_DEV_TIMEOUT and nothing
+    else (the audit finds the hand-off counters reset, so the last down CTA still
+    cleaned up), and after reset, with the stall removed, the handle decodes the
+    oracle's outputs again."""
+    import time
+    from expert_cache_router_gb300 import MoeOffloadError
+    from expert_cache_router_gb300._lib import MOE_DEV_TIMEOUT
+    from parity import check_layer
+    c = tiny.cfg
+    T = 2
+    h = tiny.handle(torch, dev)
+    try:
+        xd = _bits(tiny.x[:3, :, :T]).to(dev)
+        out = torch.empty((T, c.hidden), dtype=torch.int16, device=dev)
+        h.decode_layer(0, xd[0, 0], T, out)          # warm: kernels loaded
+        torch.cuda.synchronize()
+        h.reset()
+        h.debug_wait(limit_ns=1_000_000, stall=True)
+        t0 = time.perf_counter()
+        h.decode_layer(0, xd[0, 0], T, out)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+        assert elapsed < 0.5, elapsed
+        with pytest.raises(MoeOffloadError) as ei:
+            h.get_stats()
+        assert ei.value.status == MOE_ERR_DEVICE_STATUS
+        h.audit(0)
+        assert h.get_stats(check=False)["device_status"] == MOE_DEV_TIMEOUT
+        h.debug_wait(limit_ns=0, stall=False)
+        h.reset()
+        assert h.get_stats()["device_status"] == 0
+        for t in range(3):
+            for l in range(c.num_layers):
+                h.decode_layer(l, xd[t, l], T, out)
+                ids, w, _ = h.read_routing()
+                check_layer(out.cpu().numpy().view(np.uint16), tiny.x[t, l, :T], tiny.wr[l], tiny.w13[l],
+                            tiny.w2[l], c.top_k, c.renormalize, ids, w, ctx=(t, l))
+        assert h.get_stats()["device_status"] == 0
+    finally:
+        h.close()
+
+
+def test_debug_wait_rejects_bad_arguments(dev, tiny):
+    from expert_cache_router_gb300 import MoeOffloadError
+    h = tiny.handle(torch, dev)
+    try:
+        for lim, stall in ((-1, False), (0, 2)):
+            with pytest.raises(MoeOffloadError) as ei:
+                h._check(h._L.moe_offload_debug_wait(h.h, lim, stall))
+            assert ei.value.status == MOE_ERR_INVALID
+    finally:
+        h.close()

@@ -84,3 +84,70 @@ def test_noalloc_ffn_rejects_sizes_beyond_its_scratch(dev):
     with pytest.raises(MoeOffloadError) as ei:
         grouped_ffn_noalloc(w13, w2, E, H, I, x, ids, w, T, k, out)
     assert ei.value.status == 1 and "exceeds" in str(ei.value)
+
+
+def _noalloc_case(dev, E, k, H, I, T, seed):
+    """Seeded weights, inputs, ids and weights for one no-alloc call (device tensors + host copies)."""
+    from workload import gen
+    w13 = gen.random_bf16((E, 2 * I, H), seed=seed, std=0.02)
+    w2 = gen.random_bf16((E, H, I), seed=seed + 1, std=0.02)
+    x = gen.random_bf16((T, H), seed=seed + 2, std=1.0)
+    ids = gen.random_ids((T, k), E, seed=seed + 3)
+    w = np.random.default_rng(seed + 4).random((T, k)).astype(np.float32)
+    d = dict(w13=_bits(w13).to(dev), w2=_bits(w2).to(dev), x=_bits(x).to(dev),
+             ids=torch.from_numpy(ids.astype(np.int32)).to(dev), w=torch.from_numpy(w).to(dev))
+    return dict(w13=w13, w2=w2, x=x, ids=ids.astype(np.int32), w=w), d
+
+
+@pytest.mark.parametrize("E,k,I,T", [(8, 2, 512, 32), (2, 2, 16384, 32)])
+def test_noalloc_accepts_its_exact_limits(dev, E, k, I, T):
+    """T*k = 64 pairs (the pair limit) and T*k*I = 2^20 fp32 values (the scratch
+    limit, 4 MiB) are accepted; every row matches the oracle."""
+    import oracle
+    from expert_cache_router_gb300 import grouped_ffn_noalloc
+    from parity import assert_rows
+    H = 256
+    assert T * k == 64 and T * k * I <= 1 << 20
+    hst, d = _noalloc_case(dev, E, k, H, I, T, seed=31 + I)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.full((T, H), -1, dtype=torch.int16, device=dev)
+    grouped_ffn_noalloc(d["w13"], d["w2"], E, H, I, d["x"], d["ids"], d["w"], T, k, out, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    want, _ = oracle.moe_ffn(hst["x"], hst["ids"], hst["w"], hst["w13"], hst["w2"])
+    assert_rows(oracle.bf16_to_f32(out.cpu().numpy().view(np.uint16)), want)
+
+
+def test_noalloc_rejects_one_step_past_the_scratch_limit(dev):
+    """T*k = 64 and I = 16448: T*k*I is 64 x 64 floats past 2^20, refused before any launch."""
+    from expert_cache_router_gb300 import grouped_ffn_noalloc, MoeOffloadError
+    E, k, H, I, T = 2, 2, 256, 16448, 32
+    out = torch.full((T, H), 7, dtype=torch.int16, device=dev)
+    z = torch.zeros(16, dtype=torch.int32, device=dev)  # never read: the call is refused first
+    with pytest.raises(MoeOffloadError) as ei:
+        grouped_ffn_noalloc(z, z, E, H, I, z, z, z, T, k, out)
+    assert ei.value.status == 1 and "fixed scratch" in str(ei.value)
+    torch.cuda.synchronize()
+    assert bool((out == 7).all())
+
+
+def test_noalloc_flags_an_expert_id_outside_the_arrays(dev):
+    """An id equal to E sets MOE_DEV_BAD_SLOT_ID in the caller's status word; the
+    other tokens' rows are still computed."""
+    import oracle
+    from expert_cache_router_gb300 import grouped_ffn_noalloc
+    from expert_cache_router_gb300._lib import MOE_DEV_BAD_SLOT_ID
+    from parity import assert_rows
+    E, k, H, I, T = 8, 2, 256, 512, 4
+    hst, d = _noalloc_case(dev, E, k, H, I, T, seed=77)
+    bad = hst["ids"].copy()
+    bad[1, 0] = E
+    d["ids"] = torch.from_numpy(bad).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.zeros((T, H), dtype=torch.int16, device=dev)
+    grouped_ffn_noalloc(d["w13"], d["w2"], E, H, I, d["x"], d["ids"], d["w"], T, k, out, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & MOE_DEV_BAD_SLOT_ID
+    rows = [0, 2, 3]
+    want, _ = oracle.moe_ffn(hst["x"][rows], hst["ids"][rows], hst["w"][rows], hst["w13"], hst["w2"])
+    assert_rows(oracle.bf16_to_f32(out.cpu().numpy().view(np.uint16))[rows], want)
