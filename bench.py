@@ -32,11 +32,10 @@ sys.path.insert(0, ROOT)
 METRIC = "offloaded MoE decode tok/s at batch 1/8; misses/token; H2D & HBM GB/s vs peak"
 DTYPE_NAME = {False: "bf16", True: "fp8_e4m3_b128 weights x bf16 activations, fp32 accumulate"}
 # DRAM bytes (read + write) per launch of the two decode FFN kernels, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum, one pass) of 192 steady-state launches each
-# (timed steps 17-20, batch 1, LRU, no lookahead) of the current kernels; the command and the
-# figures are in profiles/ffn_kernels_qwen3_30b_a3b.md. Installed experts arrive over NVLink-C2C,
-# which is not DRAM traffic, and their slot writes stay in L2 within a launch. Workloads without
-# a capture report null.
+# (dram__bytes_read.sum + dram__bytes_write.sum, one pass) of steady-state launches of the
+# current kernels at batch 1 (LRU, no lookahead); the profiles directory holds the command and
+# the figures. Installed experts arrive over NVLink-C2C, which is not DRAM traffic, and their
+# slot writes stay in L2 within a launch. Workloads without a capture report null.
 NCU_DRAM_BYTES_PER_LAUNCH = {
     "qwen3_30b_a3b_L48_E128_k8_H2048_I768_S25": {"gate_up": 44.293e6 + 0.015e6, "down": 25.251e6},
 }
@@ -58,6 +57,8 @@ def parse():
     p.add_argument("--no-b8", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-sub", action="store_true",
+                   help="skip the Mixtral-8x7B-shape and FP8-lookahead sub-runs of the default workload")
     p.add_argument("--prefill-tokens", type=int, default=2048)
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--policy", choices=["lru", "static"], default="lru",
@@ -399,13 +400,214 @@ def run_reference(args, dist):
     print(json.dumps(line), flush=True)
 
 
+REPEATS = 5       # timed passes of the headline workload (median reported, min and max beside it)
+SUB_REPEATS = 3   # timed passes of each sub-workload variant
+
+
+def release_pinned():
+    """Free every host store allocated through pinned_allocator."""
+    for a in _PINNED:
+        a.close()
+    _PINNED.clear()
+
+
+class Passes:
+    """Timed decode passes of one handle: graph replays over a K-token stream,
+    each pass from an empty slot table (LRU) or from the placement (static)."""
+
+    def __init__(self, moe, dist, stream, static=False):
+        self.moe, self.dist, self.stream, self.static = moe, dist, stream, static
+
+    def restart(self):
+        if not self.static:
+            self.moe.reset()
+        return self.moe.get_stats() if self.static else None
+
+    @staticmethod
+    def delta(st, before):
+        return st if before is None else {k: st[k] - before[k] if k != "device_status" else st[k] for k in st}
+
+    def timed(self, graph, gx, xdev, K, instrument=False):
+        """K replays: (seconds max over ranks, per-phase ms sums, stats delta)."""
+        import numpy as np
+        import torch
+        before = self.restart()
+        sums = np.zeros(3)
+        self.dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for t in range(K):
+            gx.copy_(xdev[t])
+            graph.launch(self.stream)
+            if instrument:
+                sums += np.array([a.sum() for a in graph.times()], dtype=np.float64)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        self.dist.barrier()
+        return self.dist.max(e0.elapsed_time(e1) * 1e-3), sums, self.delta(self.moe.get_stats(), before)
+
+
+def decode_batch(P, cfg, B, xw, xt, xt_host, K, W, repeats, stream, full=True, sampler=None, e2e=False):
+    """One batch size: warm-up, `repeats` plain passes (pass A), and with full=True the
+    instrumented pass (B) and the misses of the first 16 tokens; e2e adds the host-buffer pass."""
+    import numpy as np
+    import torch
+    from expert_cache_router_gb300 import DecodeGraph
+    L, H = cfg.num_layers, cfg.hidden
+    moe = P.moe
+    gx = torch.zeros((L, B, H), dtype=torch.int16, device=xt.device)
+    go = torch.zeros((L, B, H), dtype=torch.int16, device=xt.device)
+    g_plain = DecodeGraph(moe, B, gx, go, timing=False)
+    for t in range(W):                          # warm-up on its own token stream
+        gx.copy_(xw[t])
+        g_plain.launch(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    runs = [P.timed(g_plain, gx, xt, K) for _ in range(repeats)]
+    clocks = sampler.stop() if sampler else None
+    secs = [r[0] for r in runs]
+    med = sorted(range(repeats), key=lambda i: secs[i])[repeats // 2]
+    r = dict(secs=secs[med], secs_all=secs, stats=runs[med][2], launches=g_plain.kernel_count * K, clocks=clocks)
+    if full:
+        g_timed = DecodeGraph(moe, B, gx, go, timing=True)
+        _, r["phase_ms"], r["stats_b"] = P.timed(g_timed, gx, xt, K, instrument=True)
+        g_timed.close()
+        before16 = P.restart()                 # misses of the first 16 tokens, for the steady state
+        n0 = min(16, K)
+        for t in range(n0):
+            gx.copy_(xt[t])
+            g_plain.launch(stream)
+        early = P.delta(moe.get_stats(), before16)["misses"]
+        r["steady_misses"] = (r["stats"]["misses"] - early) / max(K - n0, 1)
+    if e2e:
+        xh = torch.from_numpy(xt_host.view(np.int16)).pin_memory()
+        oh = torch.empty((K, L, B, H), dtype=torch.int16).pin_memory()
+        P.restart()
+        P.dist.barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for t in range(K):
+            g_plain.launch_host(xh[t], oh[t], stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        r["e2e_secs"] = P.dist.max(a.elapsed_time(b) * 1e-3)
+    g_plain.close()
+    return r
+
+
+def summarize(cfg, store, r1, K, world, link, hbm_peak, traffic=None):
+    """Throughput, misses, link bound, per-layer time split and the two FFN kernels'
+    rooflines of a batch-1 result of decode_batch(full=True)."""
+    L = cfg.num_layers
+    B_e = cfg.expert_bytes
+    h2d_gbs = link["copy_engine_gbs"]
+    stats = r1["stats"]
+    head_ms, gu_ms, dn_ms = r1["phase_ms"]
+    total_ms = head_ms + gu_ms + dn_ms
+    sb = r1["stats_b"]
+    launches = K * L                           # launches of each of the three kernels in pass B
+    installs = sb["misses"] - sb["spills"]
+    w13_b, w2_b = store.expert_split()
+    sh13_b, sh2_b = store.shared_bytes()
+    traffic = traffic or {}
+    # gate/up launch: installed experts cross the host link whole (W13 computed through, W2
+    # copied by its copy CTAs), spilled experts' W13 too; resident experts' W13 come from HBM
+    gu_host = installs * B_e + sb["spills"] * w13_b
+    # reads of resident W13 + writes into slots (+ the shared expert's W13, every layer)
+    gu_hbm = sb["hits"] * w13_b + installs * B_e + launches * sh13_b
+    dn_hbm = (sb["hits"] + installs) * w2_b + launches * sh2_b
+    dn_host = sb["spills"] * w2_b
+    gu_s, dn_s = gu_ms * 1e-3, dn_ms * 1e-3
+    gu_bound_s = max(gu_host / (h2d_gbs * 1e9), gu_hbm / (hbm_peak * 1e9) if hbm_peak else 0.0)
+    dn_bound_s = max(dn_host / (h2d_gbs * 1e9), dn_hbm / (hbm_peak * 1e9) if hbm_peak else 0.0)
+    phases = {"route_topk_ensure": head_ms, "gate_up_with_miss_copy": gu_ms, "down_combine": dn_ms}
+    gu_ach = gu_host / gu_s / 1e9 if gu_s else 0.0
+    gu_roof = {"kernel": "ffn_gate_up_kernel (moe_grouped_ffn gate/up with the miss copy folded in)",
+               "bound": "h2d", "achieved": gu_ach, "peak": h2d_gbs,
+               "unit": "GB/s", "frac": gu_ach / h2d_gbs if gu_s else None,
+               "traffic": traffic.get("gate_up"),
+               "peak_source": "pinned cudaMemcpyAsync host->device ceiling measured in this run (1 GiB copies)",
+               "frac_of_sm_read_ceiling": gu_ach / link["sm_read_gbs"] if link.get("sm_read_gbs") else None,
+               "host_bytes_per_launch": gu_host / launches, "hbm_bytes_per_launch": gu_hbm / launches,
+               "ms_per_launch": gu_ms / launches,
+               "frac_of_bound": gu_bound_s / gu_s if gu_s else None}
+    dn_roof = {"kernel": "ffn_down_combine_kernel", "bound": "hbm",
+               "achieved": dn_hbm / dn_s / 1e9 if dn_s else 0.0, "peak": hbm_peak, "unit": "GB/s",
+               "frac": (dn_hbm / dn_s / 1e9) / hbm_peak if (dn_s and hbm_peak) else None,
+               "traffic": traffic.get("down"),
+               "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)",
+               "hbm_bytes_per_launch": dn_hbm / launches, "ms_per_launch": dn_ms / launches,
+               "frac_of_bound": dn_bound_s / dn_s if dn_s else None}
+    link_bytes = stats["bytes_copied"] + stats["prefetch_bytes"]
+    secs = r1["secs"]
+    tok = [world * K / x for x in r1["secs_all"]]
+    us = 1e3 / launches
+    out = {
+        "value": world * K / secs, "unit": "tok/s", "ms_per_step": secs / K * 1e3, "tokens": K,
+        "repeats": {"n": len(tok), "median": statistics.median(tok), "min": min(tok), "max": max(tok)},
+        "misses_per_token": stats["misses"] / K,
+        "misses_per_token_steady": r1.get("steady_misses"),
+        "hit_rate": stats["hits"] / max(stats["hits"] + stats["misses"], 1),
+        "miss_bytes_per_token": stats["bytes_copied"] / K,
+        "link_bytes_per_token": link_bytes / K,
+        "copy_bound_tok_s": (h2d_gbs * 1e9) / (link_bytes / K) if link_bytes else None,
+        "frac_of_copy_bound": (world * K / secs) / ((h2d_gbs * 1e9) / (link_bytes / K)) if link_bytes else None,
+        "lookahead": {"prefetch_n": cfg.prefetch_n,
+                      "installs_per_token": stats["prefetch_installs"] / K,
+                      "hits_per_token": stats["prefetch_hits"] / K,
+                      "bytes_per_token": stats["prefetch_bytes"] / K} if cfg.prefetch_n else None,
+        "phase_share": {p: round(v / total_ms, 4) for p, v in phases.items()},
+        # per layer, from the instrumented pass (events between the launches, so no overlap):
+        # gate/up's link time is its host bytes at the copy-engine ceiling; the rest of
+        # gate/up is its start (slot ids, grouping, first host bytes) and its HBM-side work
+        "per_layer_us": {"head": head_ms * us, "gate_up": gu_ms * us,
+                         "gate_up_link_at_ceiling": gu_host / launches / (h2d_gbs * 1e9) * 1e6,
+                         "gate_up_beyond_link": gu_ms * us - gu_host / launches / (h2d_gbs * 1e9) * 1e6,
+                         "down_tail": dn_ms * us},
+        "roofline": gu_roof if gu_ms >= dn_ms else dn_roof,
+        "roofline_other": dn_roof if gu_ms >= dn_ms else gu_roof,
+        "dominant_kernel": max(phases, key=phases.get),
+        "gpu_launches": r1["launches"],
+    }
+    return out
+
+
+def sub_workload(args, base, variants, K, W, dev, stream, dist, link, hbm_peak):
+    """Another workload on the driver's clock: its own host store (freed afterwards), one
+    handle per variant (slot count or lookahead depth), SUB_REPEATS timed passes each."""
+    import numpy as np
+    import torch
+    store = Store(base, f"[rank {dist.rank}] ", allocator=pinned_allocator)
+    try:
+        router = [torch.from_numpy(store.wr[l].view(np.int16)).to(dev) for l in range(base.num_layers)]
+        xw = torch.from_numpy(store.inputs(W, 1, stream=1).view(np.int16)).to(dev)
+        xt_host = store.inputs(K, 1, stream=0)
+        xt = torch.from_numpy(xt_host.view(np.int16)).to(dev)
+        res = {}
+        for label, cfg in variants:
+            store.cfg = cfg
+            moe = store.handle(torch, dev, router, device=dist.local)
+            try:
+                r = decode_batch(Passes(moe, dist, stream), cfg, 1, xw, xt, xt_host, K, W, SUB_REPEATS, stream)
+                res[label] = dict(workload=cfg.name, slots=cfg.num_slots, prefetch_n=cfg.prefetch_n,
+                                  warmup=W, **summarize(cfg, store, r, K, dist.world, link, hbm_peak))
+            finally:
+                moe.close()
+        return res
+    finally:
+        del store
+        release_pinned()
+
+
 def run_ours(args, dist):
     import numpy as np
     import torch
     import __graft_entry__
     __graft_entry__.build()
-    from expert_cache_router_gb300 import MoeOffload, DecodeGraph
-    from workload import gen
+    from expert_cache_router_gb300 import DecodeGraph, PinnedHostArray, host_read_gbs
 
     cfg = workload(args)
     K, W = args.steps, args.warmup
@@ -429,50 +631,31 @@ def run_ours(args, dist):
     moe = store.handle(torch, dev, router, device=dist.local)
     log(f"[rank {dist.rank}] handle created in {time.time() - t0:.1f} s, "
         f"{moe.device_bytes() / 2**30:.1f} GiB on the device")
-    h2d_gbs = h2d_ceiling(torch, dev)
+    probe = PinnedHostArray((1 << 29,), np.uint16)      # 1 GiB, pinned and mapped
+    probe.array.fill(1)
+    link = {"copy_engine_gbs": h2d_ceiling(torch, dev),
+            "sm_read_gbs": host_read_gbs(probe.array, dist.local),
+            "nominal_pcie_gen5_x16_gbs": 64.0,
+            "how": "copy engine: pinned cudaMemcpyAsync host->device, 1 GiB, best of 5; SM reads: "
+                   "moe_offload_host_read_gbs (16-byte loads of pinned mapped memory, two CTAs per SM), "
+                   "1 GiB, best of 5"}
+    probe.close()
     hbm_peak = measured_peaks().get("hbm_gbs")
     stream = torch.cuda.current_stream()
 
     static = args.policy == "static"
-
-    def restart():
-        """LRU: empty every table. Static: the placement stays; counters are read as deltas."""
-        if not static:
-            moe.reset()
-        return moe.get_stats() if static else None
-
-    def delta(st, before):
-        return st if before is None else {k: st[k] - before[k] if k != "device_status" else st[k] for k in st}
-
-    def timed_pass(graph, gx, xdev, instrument=False):
-        """K replays from an empty table (LRU) or the placement (static): (seconds, phase ms sums, stats)."""
-        before = restart()
-        sums = np.zeros(3)
-        dist.barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for t in range(K):
-            gx.copy_(xdev[t])
-            graph.launch(stream)
-            if instrument:
-                sums += np.array([a.sum() for a in graph.times()], dtype=np.float64)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        dist.barrier()
-        return e0.elapsed_time(e1) * 1e-3, sums, delta(moe.get_stats(), before)
-
+    P = Passes(moe, dist, stream, static)
     placement = None
     if static:
         # Profile on its own token stream with LRU, plan the top-S experts of every layer, freeze.
         from expert_cache_router_gb300 import plan_static
-        P = args.profile_tokens
-        xp = torch.from_numpy(store.inputs(P, 1, stream=5).view(np.int16)).to(dev)
+        Pt = args.profile_tokens
+        xp = torch.from_numpy(store.inputs(Pt, 1, stream=5).view(np.int16)).to(dev)
         gx = torch.zeros((L, 1, H), dtype=torch.int16, device=dev)
         go = torch.zeros_like(gx)
         g = DecodeGraph(moe, 1, gx, go)
         moe.reset()
-        for t in range(P):
+        for t in range(Pt):
             gx.copy_(xp[t])
             g.launch(stream)
         torch.cuda.synchronize()
@@ -484,96 +667,27 @@ def run_ours(args, dist):
             moe.set_placement(l, plan)
             placed += int(counts[plan].sum())
             routed += int(counts.sum())
-        placement = {"name": "static top-S placement", "profile_tokens": P,
+        placement = {"name": "static top-S placement", "profile_tokens": Pt,
                      "profile_stream": "its own seeded stream (not the timed one)",
                      "profile_pairs_served_by_slots": placed / max(routed, 1)}
-        log(f"[rank {dist.rank}] static placement from {P} profiled tokens: "
+        log(f"[rank {dist.rank}] static placement from {Pt} profiled tokens: "
             f"{placed / max(routed, 1):.3f} of profiled pairs on slots")
 
-    results, clocks = {}, None
+    results = {}
     for B in batches:
         xw, xt, xt_host = xs[B]
-        gx = torch.zeros((L, B, H), dtype=torch.int16, device=dev)
-        go = torch.zeros((L, B, H), dtype=torch.int16, device=dev)
-        g_plain = DecodeGraph(moe, B, gx, go, timing=False)
-        g_timed = DecodeGraph(moe, B, gx, go, timing=True) if B == 1 else None
-        for t in range(W):                      # warm-up on its own token stream
-            gx.copy_(xw[t])
-            g_plain.launch(stream)
-        torch.cuda.synchronize()
-        sampler = ClockSampler(dist.local)
-        if B == 1:
-            sampler.start()
-        secs, _, stats = timed_pass(g_plain, gx, xt)
-        if B == 1:
-            clocks = sampler.stop()
-        r = dict(secs=dist.max(secs), stats=stats, launches=g_plain.kernel_count * K)
-        if B == 1:
-            _, r["phase_ms"], r["stats_b"] = timed_pass(g_timed, gx, xt, instrument=True)
-            before16 = restart()                 # misses of the first 16 tokens, for the steady state
-            n0 = min(16, K)
-            for t in range(n0):
-                gx.copy_(xt[t])
-                g_plain.launch(stream)
-            early = delta(moe.get_stats(), before16)["misses"]
-            r["steady_misses"] = (stats["misses"] - early) / max(K - n0, 1)
-            if not args.no_e2e:
-                xh = torch.from_numpy(xt_host.view(np.int16)).pin_memory()
-                oh = torch.empty((K, L, B, H), dtype=torch.int16).pin_memory()
-                restart()
-                dist.barrier()
-                torch.cuda.synchronize()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                for t in range(K):
-                    g_plain.launch_host(xh[t], oh[t], stream)
-                b.record(stream)
-                torch.cuda.synchronize()
-                r["e2e_secs"] = dist.max(a.elapsed_time(b) * 1e-3)
-            g_timed.close()
-        g_plain.close()
-        results[B] = r
+        results[B] = decode_batch(P, cfg, B, xw, xt, xt_host, K, W, REPEATS if B == 1 else 1, stream,
+                                  full=(B == 1), sampler=ClockSampler(dist.local) if B == 1 else None,
+                                  e2e=(B == 1 and not args.no_e2e))
 
     r1 = results[1]
     world = dist.world
     stats = r1["stats"]
-    head_ms, gu_ms, dn_ms = r1["phase_ms"]
-    total_ms = head_ms + gu_ms + dn_ms
-    sb = r1["stats_b"]
-    launches = K * L                               # launches of each of the three kernels in pass B
-    installs = sb["misses"] - sb["spills"]
-    w13_b, w2_b = store.expert_split()
-    sh13_b, sh2_b = store.shared_bytes()
-    # gate/up launch: installed experts cross the host link whole (W13 computed through, W2
-    # copied by its copy CTAs), spilled experts' W13 too; resident experts' W13 come from HBM
-    gu_host = installs * B_e + sb["spills"] * w13_b
-    # reads of resident W13 + writes into slots (+ the shared expert's W13, every layer)
-    gu_hbm = sb["hits"] * w13_b + installs * B_e + launches * sh13_b
-    dn_hbm = (sb["hits"] + installs) * w2_b + launches * sh2_b
-    dn_host = sb["spills"] * w2_b
-    gu_s, dn_s = gu_ms * 1e-3, dn_ms * 1e-3
-    gu_bound_s = max(gu_host / (h2d_gbs * 1e9), gu_hbm / (hbm_peak * 1e9) if hbm_peak else 0.0)
-    dn_bound_s = max(dn_host / (h2d_gbs * 1e9), dn_hbm / (hbm_peak * 1e9) if hbm_peak else 0.0)
-    phases = {"route_topk_ensure": head_ms, "gate_up_with_miss_copy": gu_ms, "down_combine": dn_ms}
     traffic = NCU_DRAM_BYTES_PER_LAUNCH.get(cfg.name, {}) if (args.policy == "lru" and not cfg.prefetch_n) else {}
-    gu_roof = {"kernel": "ffn_gate_up_kernel (moe_grouped_ffn gate/up with the miss copy folded in)",
-               "bound": "h2d", "achieved": gu_host / gu_s / 1e9 if gu_s else 0.0, "peak": h2d_gbs,
-               "unit": "GB/s", "frac": (gu_host / gu_s / 1e9) / h2d_gbs if gu_s else None,
-               "traffic": traffic.get("gate_up"),
-               "peak_source": "pinned cudaMemcpyAsync host->device ceiling measured in this run (1 GiB copies)",
-               "host_bytes_per_launch": gu_host / launches, "hbm_bytes_per_launch": gu_hbm / launches,
-               "ms_per_launch": gu_ms / launches,
-               "frac_of_bound": gu_bound_s / gu_s if gu_s else None}
-    dn_roof = {"kernel": "ffn_down_combine_kernel", "bound": "hbm",
-               "achieved": dn_hbm / dn_s / 1e9 if dn_s else 0.0, "peak": hbm_peak, "unit": "GB/s",
-               "frac": (dn_hbm / dn_s / 1e9) / hbm_peak if (dn_s and hbm_peak) else None,
-               "traffic": traffic.get("down"),
-               "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)",
-               "hbm_bytes_per_launch": dn_hbm / launches, "ms_per_launch": dn_ms / launches,
-               "frac_of_bound": dn_bound_s / dn_s if dn_s else None}
+    m = summarize(cfg, store, r1, K, world, link, hbm_peak, traffic)
     line = {
-        "metric": METRIC, "value": world * K / r1["secs"], "unit": "tok/s", "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": r1["secs"] / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": m["value"], "unit": "tok/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": m["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": DTYPE_NAME[cfg.fp8], "data": "synthetic",
         "config": {"workload": cfg.name, "batch": 1, "layers": L, "experts": cfg.num_experts, "top_k": k,
                    "host_store": "pinned mapped host memory (moe_offload_host_alloc)",
@@ -582,28 +696,19 @@ def run_ours(args, dist):
                    "host_store_gib": round(cfg.host_bytes / 2**30, 2),
                    "l2": "inputs larger than L2: each step reads %.2f GB of expert weights"
                          % ((stats["hits"] + stats["misses"]) * B_e / K / 1e9),
+                   "timing": f"value = median of {REPEATS} timed passes of K steps, each from an empty "
+                             f"slot table; min and max under repeats",
                    "parallelism": f"replicas x{world}"},
-        "misses_per_token": stats["misses"] / K,
         "slot_policy": placement if static else "lru",
-        "lookahead": {"prefetch_n": cfg.prefetch_n,
-                      "installs_per_token": stats["prefetch_installs"] / K,
-                      "hits_per_token": stats["prefetch_hits"] / K,
-                      "bytes_per_token": stats["prefetch_bytes"] / K} if cfg.prefetch_n else None,
-        "misses_per_token_steady": r1["steady_misses"],
-        "hit_rate": stats["hits"] / max(stats["hits"] + stats["misses"], 1),
-        "miss_bytes_per_token": stats["bytes_copied"] / K,
+        "link": link,
         "h2d_gbs_per_step": stats["bytes_copied"] / r1["secs"] / 1e9,
-        "link_bytes_per_token": (stats["bytes_copied"] + stats["prefetch_bytes"]) / K,
-        "copy_bound_tok_s": ((h2d_gbs * 1e9) / ((stats["bytes_copied"] + stats["prefetch_bytes"]) / K)
-                             if stats["bytes_copied"] + stats["prefetch_bytes"] else None),
-        "phase_share": {p: round(v / total_ms, 4) for p, v in phases.items()},
-        "roofline": gu_roof if gu_ms >= dn_ms else dn_roof,
-        "roofline_other": dn_roof if gu_ms >= dn_ms else gu_roof,
-        "head_us_per_layer": head_ms / launches * 1e3,
-        "dominant_kernel": max(phases, key=phases.get),
-        "gpu_launches": r1["launches"],
-        "clocks": clocks,
+        "head_us_per_layer": m["per_layer_us"]["head"],
+        "clocks": r1["clocks"],
     }
+    for key in ("repeats", "misses_per_token", "misses_per_token_steady", "hit_rate", "miss_bytes_per_token",
+                "link_bytes_per_token", "copy_bound_tok_s", "frac_of_copy_bound", "lookahead", "phase_share",
+                "per_layer_us", "roofline", "roofline_other", "dominant_kernel", "gpu_launches"):
+        line[key] = m[key]
     if 8 in results:
         r8 = results[8]
         s8 = r8["stats"]
@@ -623,6 +728,19 @@ def run_ours(args, dist):
         line["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": cores, "kind": "oracle",
                                 "sample": f"first {ntok} tokens of the timed stream at batch 1, all {L} layers "
                                           f"({dt:.1f} s)"}
+    del store
+    release_pinned()
+    if not args.no_sub and args.workload == "qwen3" and not static and not args.layers:
+        from workload import MIXTRAL_8X7B, FP8_LOOKAHEAD
+        # Mixtral-8x7B shape (S = 2 and 4) and the FP8 + lookahead workload (N = 0 and 4), each
+        # over its own configured token count and seeded streams
+        mx = MIXTRAL_8X7B
+        line["mixtral"] = sub_workload(args, mx, [(f"S{S}", replace(mx, num_slots=S)) for S in (2, 4)],
+                                       mx.decode_tokens, max(W, 3), dev, stream, dist, link, hbm_peak)
+        f8 = FP8_LOOKAHEAD
+        line["fp8_lookahead"] = sub_workload(args, f8, [(f"N{N}", replace(f8, prefetch_n=N)) for N in (0, 4)],
+                                             f8.decode_tokens, max(W, 3), dev, stream, dist, link, hbm_peak)
+    if dist.rank == 0:
         print(json.dumps(line), flush=True)
 
 

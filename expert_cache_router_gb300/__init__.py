@@ -6,8 +6,8 @@ compute path is the CUDA library libmoe_offload.so (C ABI in
 include/moe_offload.h); this package holds its build and a ctypes binding.
 """
 from .binding import (MoeOffload, MoeOffloadError, DecodeGraph, PinnedHostArray, slots_for_fraction, slots_auto,
-                      grouped_ffn_noalloc, plan_static)
+                      grouped_ffn_noalloc, plan_static, host_read_gbs)
 from . import _lib
 
 __all__ = ["MoeOffload", "MoeOffloadError", "DecodeGraph", "PinnedHostArray", "slots_for_fraction", "slots_auto",
-           "grouped_ffn_noalloc", "plan_static", "_lib"]
+           "grouped_ffn_noalloc", "plan_static", "host_read_gbs", "_lib"]

@@ -26,7 +26,7 @@ EXPORTS = [
     "moe_offload_read_slot_scales", "moe_offload_set_shared_expert", "moe_offload_reset",
     "moe_offload_host_alloc", "moe_offload_host_free", "moe_offload_prefill_times",
     "moe_offload_device_bytes", "moe_offload_get_config", "moe_offload_read_routing",
-    "moe_offload_debug_wait", "moe_offload_graph_create", "moe_offload_graph_launch",
+    "moe_offload_host_read_gbs", "moe_offload_debug_wait", "moe_offload_graph_create", "moe_offload_graph_launch",
     "moe_offload_graph_launch_host", "moe_offload_graph_times", "moe_offload_graph_kernel_count",
     "moe_offload_graph_destroy", "moe_offload_grouped_ffn_noalloc", "moe_offload_last_error",
     "moe_offload_destroy",
@@ -121,6 +121,9 @@ def _declare(L):
     L.moe_offload_get_config.argtypes = [_vp, ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_size_t)]
     L.moe_offload_read_routing.restype = _st
     L.moe_offload_read_routing.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, _ip]
+    L.moe_offload_host_read_gbs.restype = _st
+    L.moe_offload_host_read_gbs.argtypes = [ctypes.c_int, _vp, ctypes.c_size_t, ctypes.c_int,
+                                            ctypes.POINTER(ctypes.c_double)]
     L.moe_offload_debug_wait.restype = _st
     L.moe_offload_debug_wait.argtypes = [_vp, ctypes.c_longlong, ctypes.c_int]
     L.moe_offload_graph_create.restype = _st

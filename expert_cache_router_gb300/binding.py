@@ -64,6 +64,18 @@ def grouped_ffn_noalloc(w13, w2, num_experts: int, hidden: int, inter: int, x, i
         raise MoeOffloadError(st, L.moe_offload_last_error(None).decode())
 
 
+def host_read_gbs(host_array, device: int = 0, reps: int = 5) -> float:
+    """moe_offload_host_read_gbs: best GB/s of SM loads reading a pinned, mapped host
+    array (e.g. a PinnedHostArray's array) from the GPU."""
+    L = C.load()
+    g = ctypes.c_double()
+    nbytes = int(host_array.nbytes) & ~15
+    st = L.moe_offload_host_read_gbs(int(device), _ptr(host_array), nbytes, int(reps), ctypes.byref(g))
+    if st != C.MOE_OK:
+        raise MoeOffloadError(st, L.moe_offload_last_error(None).decode())
+    return float(g.value)
+
+
 def plan_static(counts, num_slots: int) -> np.ndarray:
     """moe_offload_plan_static: the num_slots most-routed experts (ties: lower id)."""
     c = np.ascontiguousarray(counts, dtype=np.uint64)

@@ -1197,6 +1197,46 @@ moe_status_t moe_offload_read_routing(moe_offload_t h, int32_t* ids, float* w, i
   return MOE_OK;
 }
 
+moe_status_t moe_offload_host_read_gbs(int device, const void* host_ptr, size_t bytes, int reps, double* best_gbs) {
+  if (!host_ptr || !best_gbs || reps < 1 || bytes < 16 || bytes % 16 != 0 || !aligned16(host_ptr))
+    return fail(nullptr, MOE_ERR_INVALID, "host_read_gbs: NULL, unaligned or empty buffer, or reps < 1");
+  *best_gbs = 0.0;
+  cudaError_t e = cudaSetDevice(device);
+  void* dp = nullptr;
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dp, const_cast<void*>(host_ptr), 0);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(nullptr, MOE_ERR_INVALID, "host_read_gbs: not pinned, mapped host memory: %s", cudaGetErrorString(e));
+  }
+  int sms = 0;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device)) != cudaSuccess)
+    return fail(nullptr, MOE_ERR_CUDA, "host_read_gbs: %s", cudaGetErrorString(e));
+  unsigned* sink = nullptr;
+  cudaEvent_t a = nullptr, b = nullptr;
+  cudaStream_t st = nullptr;
+  e = cudaMalloc(&sink, sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaEventCreate(&a);
+  if (e == cudaSuccess) e = cudaEventCreate(&b);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+  float best = 0.0f;
+  for (int r = 0; r <= reps && e == cudaSuccess; ++r) {  // the first read is a warm-up
+    e = cudaEventRecord(a, st);
+    if (e == cudaSuccess) e = launch_host_touch(dp, bytes, sink, 2 * sms, st);
+    if (e == cudaSuccess) e = cudaEventRecord(b, st);
+    if (e == cudaSuccess) e = cudaEventSynchronize(b);
+    float ms = 0.0f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, a, b);
+    if (e == cudaSuccess && r > 0 && (best == 0.0f || ms < best)) best = ms;
+  }
+  if (st) cudaStreamDestroy(st);
+  if (a) cudaEventDestroy(a);
+  if (b) cudaEventDestroy(b);
+  if (sink) cudaFree(sink);
+  if (e != cudaSuccess) return fail(nullptr, MOE_ERR_CUDA, "host_read_gbs: %s", cudaGetErrorString(e));
+  *best_gbs = (double)bytes / ((double)best * 1e-3) / 1e9;
+  return MOE_OK;
+}
+
 moe_status_t moe_offload_debug_wait(moe_offload_t h, long long limit_ns, int stall) {
   if (!h) return MOE_ERR_INVALID;
   if (limit_ns < 0 || (stall != 0 && stall != 1))

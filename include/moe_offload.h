@@ -417,6 +417,16 @@ moe_status_t moe_offload_get_config(moe_offload_t h, moe_offload_config_t* cfg, 
 moe_status_t moe_offload_read_routing(moe_offload_t h, int32_t* ids, float* w, int32_t* slot_ids, int cap,
                                       int* n_pairs);
 
+/* Zero-copy read ceiling of the host link (no counterpart on the pages; the
+ * miss copy's SM loads are measured against it): reads `bytes` (a multiple of
+ * 16) of pinned, mapped host memory at host_ptr (16-byte aligned) from `device`
+ * with 16-byte SM loads over a grid of two CTAs per SM, once to warm up and then
+ * `reps` times, and returns the best rate in GB/s (1e9 bytes per second).
+ * Synchronises; allocates 4 device bytes and frees them. Errors:
+ * MOE_ERR_INVALID (arguments, or memory that is not pinned and mapped; reason in
+ * moe_offload_last_error(NULL)), MOE_ERR_CUDA. */
+moe_status_t moe_offload_host_read_gbs(int device, const void* host_ptr, size_t bytes, int reps, double* best_gbs);
+
 /* Bounded waits, for tests that make one run out (no counterpart on the pages).
  * In a decode step the down launch waits per expert group, on counters the
  * gate/up CTAs raise, for at most limit_ns (0 = the default, 2 s) per wait;
@@ -508,7 +518,7 @@ moe_status_t moe_offload_grouped_ffn_noalloc(const void* w13, const void* w2, in
 
 /* One-line reason of the last failed call on this handle ("" when none). With
  * h == NULL: the reason of the last failed call that takes no handle
- * (moe_offload_create, moe_offload_grouped_ffn_noalloc) on this thread. */
+ * (moe_offload_create, moe_offload_host_read_gbs, moe_offload_grouped_ffn_noalloc) on this thread. */
 const char* moe_offload_last_error(moe_offload_t h);
 
 /* Free everything the handle owns and unregister host memory it registered.
