@@ -94,7 +94,8 @@ static __device__ __forceinline__ void ensure_load_table(EnsureSmem& sm, const L
 
 // The whole slot-table update of one call, run by one CTA of kEnsureThreads
 // threads (every thread must call it) after ensure_load_table and a barrier.
-// ids may have been written by this CTA before that barrier.
+// ids (global or shared memory) may have been written by this CTA before that
+// barrier.
 static __device__ void ensure_block(EnsureSmem& sm, LayerTables tab, const int32_t* ids, int Tk, int E, int S,
                                     int32_t* slot_ids, uint32_t* status, unsigned long long expert_bytes) {
   const int tid = threadIdx.x;
@@ -196,12 +197,13 @@ static __device__ void ensure_block(EnsureSmem& sm, LayerTables tab, const int32
     tab.counts[kCntSpill] = spills;
     tab.counts[kCntInstall] = installs;
     tab.counts[kCntDistinct] = hits + misses;
-    tab.stats[kStatCalls] += 1ull;
-    tab.stats[kStatHits] += (unsigned long long)hits;
-    tab.stats[kStatMisses] += (unsigned long long)misses;
-    tab.stats[kStatSpills] += (unsigned long long)spills;
-    tab.stats[kStatBytesCopied] += (unsigned long long)installs * expert_bytes;
-    tab.stats[kStatPrefetchHits] += (unsigned long long)sm.s_pf_hits;
+    // counters by atomic adds whose results are not used: no read round trip
+    atomicAdd(&tab.stats[kStatCalls], 1ull);
+    atomicAdd(&tab.stats[kStatHits], (unsigned long long)hits);
+    atomicAdd(&tab.stats[kStatMisses], (unsigned long long)misses);
+    atomicAdd(&tab.stats[kStatSpills], (unsigned long long)spills);
+    atomicAdd(&tab.stats[kStatBytesCopied], (unsigned long long)installs * expert_bytes);
+    atomicAdd(&tab.stats[kStatPrefetchHits], (unsigned long long)sm.s_pf_hits);
     if (sm.s_bad) atomicOr(status, kDevBadExpertId);
   }
 }
@@ -310,8 +312,8 @@ static __device__ void install_block(EnsureSmem& sm, LayerTables tab, const int*
   if (tid == 0) {
     tab.counts[kCntPrefetch] = ninst;
     tab.counts[kCntCandidates] = ncand;
-    tab.stats[kStatPrefetchInstalls] += (unsigned long long)ninst;
-    tab.stats[kStatPrefetchBytes] += (unsigned long long)ninst * expert_bytes;
+    atomicAdd(&tab.stats[kStatPrefetchInstalls], (unsigned long long)ninst);
+    atomicAdd(&tab.stats[kStatPrefetchBytes], (unsigned long long)ninst * expert_bytes);
   }
   __syncthreads();
 }

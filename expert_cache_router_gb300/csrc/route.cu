@@ -312,80 +312,143 @@ route_ensure_kernel(RouteEnsureArgs a) {
 constexpr int kClusterMaxCtas = 8;
 constexpr int kClusterMaxLogits = 2048;
 
-// Top-k of rows [T][E] of logits in shared memory, two ways with the same rule
-// (larger, or equal with a lower expert id, NaN ranking last: the rule of
-// topk_row_warp and of route_ensure_kernel). Small T*E: every candidate counts
-// the logits that beat it, P threads per candidate. Otherwise one warp per
-// token keeps its row in registers (E <= 32 * kTopkPerLane) and takes k
-// rounds of a warp arg-max. Pick r of token t lands in ids[t*k + r] (and vals).
-// Every thread of the block calls it.
-constexpr int kTopkPerLane = 8;
-constexpr int kRankMaxItems = 128;  // T*E at or below this: the block-wide rank
+// Top-k of rows [T][E] of logits in shared memory with the rule of
+// topk_row_warp and route_ensure_kernel (larger logit first, equal logits by
+// lower expert id, NaN ranking as -inf), one warp per token. Each (logit,
+// expert) pair becomes one 64-bit key whose unsigned order is that rule: the
+// logit's bits mapped to an order-preserving unsigned integer (NaN read as
+// -inf, -0 as +0) in the high word, the complement of the expert id in the low
+// word. Lane i holds the keys of experts i*M .. i*M+M-1 (0 beyond E, below
+// every real key) and sorts them in registers; then a butterfly over the lanes
+// keeps, at every step, the M largest keys of the two lists it joins
+// (elementwise max of one list and the other reversed is a bitonic sequence
+// holding exactly those, which a bitonic merge sorts). After log2 of the lanes
+// in use every lane holds the row's M largest keys in descending order, so pick
+// j is the j-th list entry.
+__device__ __forceinline__ unsigned long long rank_key(float v, int e) {
+  if (v != v) v = -INFINITY;
+  if (v == 0.0f) v = 0.0f;  // -0 ranks with +0
+  uint32_t b = __float_as_uint(v);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)b << 32) | (unsigned long long)(~(uint32_t)e);
+}
+__device__ __forceinline__ float key_value(unsigned long long key) {
+  const uint32_t b = (uint32_t)(key >> 32);
+  return __uint_as_float((b & 0x80000000u) ? (b & 0x7fffffffu) : ~b);
+}
+__device__ __forceinline__ int key_expert(unsigned long long key) { return (int)(~(uint32_t)key); }
 
-__device__ __forceinline__ void topk_rows_block(const float* lg, int T, int E, int k, int* ids, float* vals) {
-  const int n = T * E;
-  if (n <= kRankMaxItems) {
-    int P = 1;
-    while (P < 32 && n * P * 2 <= kEnsureThreads) P <<= 1;
-    const int g = threadIdx.x, idx = g / P, part = g - (g / P) * P;
-    int cnt = 0, t = 0, ee = 0;
-    float v = -INFINITY;
-    if (idx < n) {
-      t = idx / E;
-      ee = idx - t * E;
-      v = lg[idx];
-      if (v != v) v = -INFINITY;
-      const float* rw = lg + t * E;
-      for (int e2 = part; e2 < E; e2 += P) {
-        float v2 = rw[e2];
-        if (v2 != v2) v2 = -INFINITY;
-        cnt += (v2 > v) || (v2 == v && e2 < ee);
+template <int M>
+__device__ __forceinline__ void sort_desc(unsigned long long (&a)[M]) {
+#pragma unroll
+  for (int size = 2; size <= M; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < M; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const unsigned long long x = a[i], y = a[j];
+          const bool sw = (i & size) == 0 ? (x < y) : (x > y);
+          a[i] = sw ? y : x;
+          a[j] = sw ? x : y;
+        }
       }
     }
-    for (int o = 1; o < P; o <<= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    if (idx < n && part == 0 && cnt < k) {
-      ids[t * k + cnt] = ee;
-      if (vals) vals[t * k + cnt] = v;
-    }
-    return;
   }
-  const int lane = threadIdx.x & 31;
-  for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5) {
-    const float* row = lg + t * E;
-    float v[kTopkPerLane];
+}
+
+// Both lanes of a butterfly pair end with the M largest keys of their two lists, descending.
+template <int M>
+__device__ __forceinline__ void keep_top_of_pair(unsigned long long (&a)[M], int s) {
+  unsigned long long b[M];
 #pragma unroll
-    for (int j = 0; j < kTopkPerLane; ++j) {
-      const int e = lane + 32 * j;
-      float x = e < E ? row[e] : -INFINITY;
-      if (x != x) x = -INFINITY;
-      v[j] = x;
+  for (int i = 0; i < M; ++i) {
+    const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)a[i], s);
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(a[i] >> 32), s);
+    b[i] = ((unsigned long long)hi << 32) | lo;
+  }
+#pragma unroll
+  for (int i = 0; i < M; ++i) a[i] = a[i] > b[M - 1 - i] ? a[i] : b[M - 1 - i];
+#pragma unroll
+  for (int stride = M >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+      const int j = i ^ stride;
+      if (j > i && a[i] < a[j]) {
+        const unsigned long long x = a[i];
+        a[i] = a[j];
+        a[j] = x;
+      }
     }
-    unsigned taken = 0u;
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
+  }
+}
+
+// The warp's top-k (k <= M) of one row lg[0..E) (shared memory), E <= 32 * M.
+// Lane j < k returns the key of pick j. The butterfly runs over at least k
+// lanes, so that lanes 0..k-1 all hold the final list.
+template <int M>
+__device__ __forceinline__ unsigned long long warp_topk_row(const float* lg, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long a[M];
 #pragma unroll
-      for (int j = 0; j < kTopkPerLane; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && !(taken >> j & 1u) && better(v[j], e, bv, bi)) {
-          bv = v[j];
-          bi = e;
-        }
-      }
+  for (int q = 0; q < M; ++q) {
+    const int e = lane * M + q;
+    a[q] = e < E ? rank_key(lg[e], e) : 0ull;
+  }
+  sort_desc<M>(a);
+  const int lanes = (E + M - 1) / M;
+  for (int s = 1; s < lanes || s < k; s <<= 1) keep_top_of_pair<M>(a, s);
+  unsigned long long mine = 0ull;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == 0) {
-        ids[t * k + r] = bi;
-        if (vals) vals[t * k + r] = bv;
-      }
+  for (int q = 0; q < M; ++q)
+    if (q == lane) mine = a[q];
+  return mine;
+}
+
+// The same picks for k > 8 (E <= 256): k rounds of a warp-wide maximum of the
+// keys not yet taken (lane i holds experts i, i+32, ...), which needs fewer
+// registers than a 16-entry list. Lane j < k returns the key of pick j.
+__device__ __forceinline__ unsigned long long warp_topk_rounds(const float* lg, int E, int k) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = lane + 32 * j;
+    v[j] = e < E ? rank_key(lg[e], e) : 0ull;
+  }
+  unsigned taken = 0u;
+  unsigned long long mine = 0ull;
+  for (int r = 0; r < k; ++r) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (!(taken >> j & 1u) && v[j] > best) best = v[j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)best, o);
+      const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(best >> 32), o);
+      const unsigned long long b = ((unsigned long long)hi << 32) | lo;
+      best = b > best ? b : best;
+    }
+    const int e = key_expert(best);
+    if ((e & 31) == lane) taken |= 1u << (e >> 5);
+    if (r == lane) mine = best;
+  }
+  return mine;
+}
+
+// Top-k of every token of lg [T][E] (shared memory), one warp per token:
+// ids[t*k + j] (and vals, when given) receive pick j. Every thread calls it;
+// E <= 256, k <= 16.
+__device__ __forceinline__ void topk_rows_warps(const float* lg, int T, int E, int k, int* ids, float* vals) {
+  const int lane = threadIdx.x & 31;
+  const bool small = k <= 8;
+  for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5) {
+    const unsigned long long key = small ? warp_topk_row<8>(lg + t * E, E, k) : warp_topk_rounds(lg + t * E, E, k);
+    if (lane < k) {
+      ids[t * k + lane] = key_expert(key);
+      if (vals) vals[t * k + lane] = key_value(key);
     }
   }
 }
@@ -406,7 +469,8 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   const bool pf = a.pf_n > 0;
   const int tc = T < TC ? T : TC;
   uint16_t* xs = reinterpret_cast<uint16_t*>(dyn);                  // [tc][H] bf16: this chunk's x
-  int* pid = reinterpret_cast<int*>(xs + (size_t)tc * H);           // [T][k] predicted ids (CTA 1)
+  int* ids_s = reinterpret_cast<int*>(xs + (size_t)tc * H);         // [T][k] routed ids (CTA 0)
+  int* pid = ids_s + T * k;                                         // [T][k] predicted ids (CTA 1)
   int* cand = pid + T * k;                                          // [T][k] candidates (CTA 1)
   // Every CTA must have started before another writes into its shared memory:
   // arrive now, wait just before the first remote store.
@@ -480,7 +544,7 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   cluster.sync();  // every logit is in CTA 0's (and predicted ones in CTA 1's) shared memory
   if (pf && crank == 1) {
     // Lookahead into the next layer: predicted top-k, candidates, install.
-    topk_rows_block(lall, T, E, k, pid, nullptr);
+    topk_rows_warps(lall, T, E, k, pid, nullptr);
     __syncthreads();
     const int nc = lookahead_candidates_block(sm, pid, lall, T, k, E, cand);
     install_block(sm, a.tab_next, cand, nc, a.pf_n, E, a.S, a.pf_bytes, true);
@@ -488,39 +552,43 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   }
   if (crank != 0) return;
 
-  int* sel_id = sm.slot_by_rank;
-  float* sel_v = reinterpret_cast<float*>(sm.key);
-  topk_rows_block(lall, T, E, k, sel_id, sel_v);
-  __syncthreads();
+  // Each token's top-k and weights in one warp; the picks go to the caller's ids
+  // and weights and, for the slot update, to shared memory.
+  const bool small = k <= 8;
   for (int t = warp; t < T; t += kEnsureThreads / 32) {
-    const float lmax = sel_v[t * k];
-    const float ej = lane < k ? expf(sel_v[t * k + lane] - lmax) : 0.0f;
+    const float* row = lall + t * E;
+    const unsigned long long key = small ? warp_topk_row<8>(row, E, k) : warp_topk_rounds(row, E, k);
+    const float v = key_value(key);
+    const float lmax = __shfl_sync(0xffffffffu, v, 0);
+    const float ej = lane < k ? expf(v - lmax) : 0.0f;
     float denom = 0.0f;
     if (r.renorm) {
       for (int j = 0; j < k; ++j) denom += __shfl_sync(0xffffffffu, ej, j);
     } else {
       float part = 0.0f;
       for (int q = lane; q < E; q += 32) {
-        float v = lall[t * E + q];
-        if (v != v) v = -INFINITY;
-        part += expf(v - lmax);
+        float lv = row[q];
+        if (lv != lv) lv = -INFINITY;
+        part += expf(lv - lmax);
       }
       denom = warp_sum(part);
     }
     if (lane < k) {
-      r.ids[(size_t)t * k + lane] = sel_id[t * k + lane];
+      const int e = key_expert(key);
+      r.ids[(size_t)t * k + lane] = e;
       r.w[(size_t)t * k + lane] = ej / denom;
+      ids_s[t * k + lane] = e;
     }
   }
   __syncthreads();
-  ensure_block(sm, a.tab, r.ids, T * k, E, a.S, a.slot_ids, a.status, a.expert_bytes);
+  ensure_block(sm, a.tab, ids_s, T * k, E, a.S, a.slot_ids, a.status, a.expert_bytes);
 }
 
 }  // namespace
 
 // Dynamic shared memory of the cluster head: x of one token chunk [TC][H] bf16,
 // then with the lookahead on predicted ids and candidates [T][k] each.
-constexpr int kHeadPredSmemMax = kTokChunk * 8192 * 2 + 2 * 1024 * 4;
+constexpr int kHeadPredSmemMax = kTokChunk * 8192 * 2 + 3 * 1024 * 4;
 
 cudaError_t route_init_attributes() {
   cudaError_t e = cudaFuncSetAttribute(route_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -562,7 +630,8 @@ cudaError_t launch_route_ensure(const RouteEnsureArgs& a, cudaStream_t st) {
     cfg.gridDim = dim3(cgrid);
     cfg.blockDim = dim3(kEnsureThreads);
     const int tc = a.r.T == 1 ? 1 : min(a.r.T, kTokChunk);
-    cfg.dynamicSmemBytes = (size_t)tc * a.r.H * 2 + (a.pf_n > 0 ? (size_t)(2 * a.r.T * a.r.k) * 4 : 0);
+    cfg.dynamicSmemBytes = (size_t)tc * a.r.H * 2 + (size_t)(a.r.T * a.r.k) * 4 +
+                           (a.pf_n > 0 ? (size_t)(2 * a.r.T * a.r.k) * 4 : 0);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -151,3 +151,36 @@ def test_empty_calls_do_nothing(dev):
         assert np.all(se == -1) and clock == 0
     finally:
         h.close()
+
+
+@pytest.mark.parametrize("k,T", [(12, 4), (16, 2), (8, 16)])
+def test_cluster_head_topk_equals_route_topk(dev, k, T):
+    """The fused cluster head's top-k (an 8-entry bitonic list per warp for k <= 8,
+    k rounds of a warp maximum above) gives the same ids and weights, bit for bit,
+    as the standalone route_topk kernel, and its slot table matches the simulator
+    replaying those ids; outputs match the oracle on every row."""
+    from oracle import SlotCacheSim
+    cfg = Workload(name=f"edge_E64_k{k}_H256_I64", config_id=95, num_layers=2, num_experts=64, top_k=k,
+                   hidden=256, inter=64, num_slots=max(k, 20), batches=(T,), decode_tokens=3, rho=0.9, skew=False)
+    st = Stack(cfg, tokens=3, batch=T)
+    h = st.handle(torch, dev, max_tokens_graph=T)
+    sims = [SlotCacheSim(cfg.num_experts, cfg.num_slots) for _ in range(cfg.num_layers)]
+    try:
+        xd = _bits(st.x[:3, :, :T]).to(dev)
+        out = torch.empty((T, cfg.hidden), dtype=torch.int16, device=dev)
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        for t in range(3):
+            for l in range(cfg.num_layers):
+                h.decode_layer(l, xd[t, l], T, out)
+                gids, gw, gslot = h.read_routing()
+                h.route_topk(l, xd[t, l], T, ids, w)
+                torch.cuda.synchronize()
+                assert np.array_equal(gids, ids.cpu().numpy()), (t, l)
+                assert np.array_equal(gw.view(np.uint32), w.cpu().numpy().view(np.uint32)), (t, l)
+                assert np.array_equal(gslot, sims[l].ensure(gids).slot_ids), (t, l)
+                check_layer(_u16(out), st.x[t, l, :T], st.wr[l], st.w13[l], st.w2[l], k, cfg.renormalize, gids, gw,
+                            ctx=(t, l))
+        assert h.get_stats()["device_status"] == 0
+    finally:
+        h.close()
