@@ -65,11 +65,28 @@ struct LayerWeights {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// L2 eviction policy for router loads: the routers of all layers (tens of MB)
+// are read every decode step and should survive the expert weights streaming
+// through L2 (gigabytes per step; an evict-first hint on those measured slower).
+__device__ __forceinline__ unsigned long long l2_evict_last() {
+  unsigned long long p;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // 16-byte read-only load that does not allocate in L1 (streamed weights).
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// 16-byte read-only load of router weights: no L1 allocation, kept in L2 across steps.
+__device__ __forceinline__ uint4 ld_keep(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(l2_evict_last()));
   return v;
 }
 

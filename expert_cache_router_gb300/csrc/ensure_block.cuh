@@ -92,8 +92,8 @@ static __device__ __forceinline__ void ensure_load_table(EnsureSmem& sm, const L
   }
 }
 
-// The whole slot-table update of one call, run by one CTA of kEnsureThreads
-// threads (every thread must call it) after ensure_load_table and a barrier.
+// The whole slot-table update of one call, run by one CTA (every thread must
+// call it; at least max(E, S) threads) after ensure_load_table and a barrier.
 // ids (global or shared memory) may have been written by this CTA before that
 // barrier.
 static __device__ void ensure_block(EnsureSmem& sm, LayerTables tab, const int32_t* ids, int Tk, int E, int S,
@@ -103,7 +103,7 @@ static __device__ void ensure_block(EnsureSmem& sm, LayerTables tab, const int32
   if (tid < S) sm.used[tid] = 0;
   if (tid == 0) { sm.s_hits = 0; sm.s_pf_hits = 0; sm.s_bad = 0u; }
   __syncthreads();
-  for (int p = tid; p < Tk; p += kEnsureThreads) {
+  for (int p = tid; p < Tk; p += blockDim.x) {
     const int e = ids[p];
     if (e >= 0 && e < E) {
       sm.present[e] = 1;
@@ -172,7 +172,7 @@ static __device__ void ensure_block(EnsureSmem& sm, LayerTables tab, const int32
 
   // Rewrite expert ids to slot ids (or spill markers); record which pairs' experts come
   // from host memory in this call (installed or spilled).
-  for (int p = tid; p < Tk; p += kEnsureThreads) {
+  for (int p = tid; p < Tk; p += blockDim.x) {
     const int e = ids[p];
     int s = -1, src = -1;
     if (e >= 0 && e < E) {

@@ -129,7 +129,7 @@ route_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__
     for (int t = 0; t < kTokChunk; ++t) acc[t] = 0.0f;
     const uint16_t* row = wr + (size_t)e * H;
     for (int c = lane * 8; c < H; c += 256) {
-      const uint4 wv = ld_stream(row + c);
+      const uint4 wv = ld_keep(row + c);
 #pragma unroll
       for (int t = 0; t < kTokChunk; ++t)
         if (t < nt) acc[t] = dot8(wv, xs + t * H + c, acc[t]);
@@ -190,7 +190,7 @@ route_ensure_kernel(RouteEnsureArgs a) {
   const uint16_t* row = r.wr + (size_t)(e < E ? e : 0) * H;
   if (e < E)
     for (int c = lane * 64; c < H; c += 32 * 64)  // one prefetch per 128-byte line
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(row + c));
+      asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(row + c));
   pdl_wait();
   pdl_trigger();
   if (e < E) {
@@ -204,7 +204,7 @@ route_ensure_kernel(RouteEnsureArgs a) {
 #pragma unroll
         for (int u = 0; u < kRowUnroll; ++u) {
           const int c = c0 + 256 * u;
-          wv[u] = c < H ? ld_stream(row + c) : make_uint4(0u, 0u, 0u, 0u);
+          wv[u] = c < H ? ld_keep(row + c) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < kRowUnroll; ++u) {
@@ -292,39 +292,54 @@ route_ensure_kernel(RouteEnsureArgs a) {
   if (threadIdx.x == 0) *r.done = 0u;
 }
 
-// Cluster variant of the fused head (E <= 32 * kClusterMaxCtas, T*E <=
-// kClusterMaxLogits): one thread-block cluster, one CTA per 32 experts. Each
-// warp stores its logits straight into CTA 0's shared memory (distributed
-// shared memory: no global round trip, fence or counter); after one cluster
-// barrier CTA 0 takes each token's top-k (topk_rows_block) and updates the slot
+// Cluster variant of the fused head (E <= 256, T*E <= kClusterMaxLogits, T*k <=
+// kHeadThreads): one thread-block cluster of up to eight CTAs, each owning a
+// contiguous range of at most 32 experts, one warp per expert. Each warp copies
+// its router row into shared memory (cp.async) before the dependency wait, so
+// that once x is in the dot products read only shared memory (a CTA of this
+// size cannot become resident beside the preceding kernel's CTAs, so the copy
+// overlaps at least the launch and the wait). Each warp stores its logits
+// straight into CTA 0's shared memory (distributed shared memory: no global
+// round trip, fence or counter);
+// after one cluster barrier CTA 0 takes each token's top-k and updates the slot
 // table while the other CTAs exit. Same picks, weights and table as the other
 // head kernels.
 //
 // With the router lookahead on (a.pf_n > 0, at least two CTAs), each warp also
-// dots the next layer's router row of its expert with the same x (the
-// predictor) and stores it into CTA 1's shared memory, and CTA 1 does the rest
-// of the lookahead while CTA 0 does the demand side: it copies the next layer's
-// table into its shared memory before the dependency wait, takes the predicted
-// top-k (the same rule as the demand top-k), orders the candidates and installs
-// them (lookahead_candidates_block, install_block). The two CTAs write
-// different layers' tables. Dynamic shared memory: x of one token chunk [TC][H]
-// (read once per CTA, not once per warp), predicted ids [T][k], candidates [T][k].
+// dots the next layer's router rows of its experts with the same x (the
+// predictor, rows pulled into L2 before the wait) and stores them into CTA 1's
+// shared memory, and CTA 1 does the rest of the lookahead while CTA 0 does the
+// demand side: it copies the next layer's table into its shared memory before
+// the dependency wait, takes the predicted top-k (the same rule as the demand
+// top-k), orders the candidates and installs them (lookahead_candidates_block,
+// install_block). The two CTAs write different layers' tables. Dynamic shared
+// memory: x of one token chunk [TC][H] (read once per CTA), routed ids,
+// predicted ids and candidates [T][k] each, the CTA's router rows [32][H].
 constexpr int kClusterMaxCtas = 8;
 constexpr int kClusterMaxLogits = 2048;
+constexpr int kRowSmemH = 2048;  // router rows staged in shared memory up to this hidden size
+constexpr int kHeadThreads = 1024;
+constexpr int kHeadWarps = kHeadThreads / 32;
+constexpr int kHeadMaxEpc = 32;  // experts per CTA of the cluster head
+
+// CTAs of the cluster head for E experts (up to eight, one warp per expert).
+__host__ __device__ inline int head_ctas(int E) {
+  const int c = (E + 31) / 32;
+  return c < 1 ? 1 : (c > kClusterMaxCtas ? kClusterMaxCtas : c);
+}
 
 // Top-k of rows [T][E] of logits in shared memory with the rule of
 // topk_row_warp and route_ensure_kernel (larger logit first, equal logits by
-// lower expert id, NaN ranking as -inf), one warp per token. Each (logit,
-// expert) pair becomes one 64-bit key whose unsigned order is that rule: the
-// logit's bits mapped to an order-preserving unsigned integer (NaN read as
-// -inf, -0 as +0) in the high word, the complement of the expert id in the low
-// word. Lane i holds the keys of experts i*M .. i*M+M-1 (0 beyond E, below
-// every real key) and sorts them in registers; then a butterfly over the lanes
-// keeps, at every step, the M largest keys of the two lists it joins
-// (elementwise max of one list and the other reversed is a bitonic sequence
-// holding exactly those, which a bitonic merge sorts). After log2 of the lanes
-// in use every lane holds the row's M largest keys in descending order, so pick
-// j is the j-th list entry.
+// lower expert id, NaN ranking as -inf). Each (logit, expert) pair becomes one
+// 64-bit key whose unsigned order is that rule: the logit's bits mapped to an
+// order-preserving unsigned integer (NaN read as -inf, -0 as +0) in the high
+// word, the complement of the expert id in the low word; 0 (below every real
+// key) pads. Two stages, so that no single warp runs a long dependent chain:
+// (1) one warp per (token, group of 32 experts) sorts the group's keys with a
+// bitonic network across its lanes and keeps the K8 largest (K8 = 8 for k <= 8,
+// else 16); (2) one warp per token sorts its groups' G*K8 candidates the same
+// way, and pick j is element j. The k largest keys of a row are among the K8
+// largest of their groups, so the picks are those of the one-stage rule.
 __device__ __forceinline__ unsigned long long rank_key(float v, int e) {
   if (v != v) v = -INFINITY;
   if (v == 0.0f) v = 0.0f;  // -0 ranks with +0
@@ -338,123 +353,90 @@ __device__ __forceinline__ float key_value(unsigned long long key) {
 }
 __device__ __forceinline__ int key_expert(unsigned long long key) { return (int)(~(uint32_t)key); }
 
-template <int M>
-__device__ __forceinline__ void sort_desc(unsigned long long (&a)[M]) {
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+// Bitonic sort, descending, of the 32*R keys one warp holds R per lane (element
+// lane*R + r): compare-exchanges within a lane for strides below R, across
+// lanes (xor of stride/R) above.
+template <int R>
+__device__ __forceinline__ void warp_sort_desc(unsigned long long (&a)[R]) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int size = 2; size <= M; size <<= 1) {
+  for (int size = 2; size <= 32 * R; size <<= 1) {
 #pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride < R) {
 #pragma unroll
-      for (int i = 0; i < M; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const unsigned long long x = a[i], y = a[j];
-          const bool sw = (i & size) == 0 ? (x < y) : (x > y);
-          a[i] = sw ? y : x;
-          a[j] = sw ? x : y;
+        for (int r = 0; r < R; ++r) {
+          const int j = r ^ stride;
+          if (j > r) {
+            const bool desc = ((lane * R + r) & size) == 0;
+            const unsigned long long x = a[r], y = a[j];
+            const bool sw = desc ? (x < y) : (x > y);
+            a[r] = sw ? y : x;
+            a[j] = sw ? x : y;
+          }
+        }
+      } else {
+        const int ls = stride / R;
+        const bool lower = (lane & ls) == 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const unsigned long long b = shfl_xor_u64(a[r], ls);
+          const bool keep_max = (((lane * R + r) & size) == 0) == lower;
+          a[r] = keep_max ? (a[r] > b ? a[r] : b) : (a[r] < b ? a[r] : b);
         }
       }
     }
   }
 }
 
-// Both lanes of a butterfly pair end with the M largest keys of their two lists, descending.
-template <int M>
-__device__ __forceinline__ void keep_top_of_pair(unsigned long long (&a)[M], int s) {
-  unsigned long long b[M];
-#pragma unroll
-  for (int i = 0; i < M; ++i) {
-    const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)a[i], s);
-    const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(a[i] >> 32), s);
-    b[i] = ((unsigned long long)hi << 32) | lo;
-  }
-#pragma unroll
-  for (int i = 0; i < M; ++i) a[i] = a[i] > b[M - 1 - i] ? a[i] : b[M - 1 - i];
-#pragma unroll
-  for (int stride = M >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-    for (int i = 0; i < M; ++i) {
-      const int j = i ^ stride;
-      if (j > i && a[i] < a[j]) {
-        const unsigned long long x = a[i];
-        a[i] = a[j];
-        a[j] = x;
-      }
-    }
+// Stage 1: every (token, group) of lg [T][E] (shared memory), one warp each; the
+// group's K8 largest keys, descending, go to cand[(t*G + g)*K8 ..]. Every thread
+// calls it; the caller synchronises before stage 2.
+__device__ __forceinline__ void topk_stage1(const float* lg, int T, int E, int K8, unsigned long long* cand) {
+  const int lane = threadIdx.x & 31;
+  const int G = (E + 31) >> 5;
+  for (int q = threadIdx.x >> 5; q < T * G; q += blockDim.x >> 5) {
+    const int t = q / G, g = q - t * G;
+    const int e = g * 32 + lane;
+    unsigned long long a[1] = {e < E ? rank_key(lg[t * E + e], e) : 0ull};
+    warp_sort_desc<1>(a);
+    if (lane < K8) cand[q * K8 + lane] = a[0];
   }
 }
 
-// The warp's top-k (k <= M) of one row lg[0..E) (shared memory), E <= 32 * M.
-// Lane j < k returns the key of pick j. The butterfly runs over at least k
-// lanes, so that lanes 0..k-1 all hold the final list.
-template <int M>
-__device__ __forceinline__ unsigned long long warp_topk_row(const float* lg, int E, int k) {
+// Stage 2 for one token: the warp sorts its n <= 32*R candidates c[0..n);
+// lane j returns the key of pick j.
+template <int R>
+__device__ __forceinline__ unsigned long long topk_stage2_r(const unsigned long long* c, int n) {
   const int lane = threadIdx.x & 31;
-  unsigned long long a[M];
+  unsigned long long a[R];
 #pragma unroll
-  for (int q = 0; q < M; ++q) {
-    const int e = lane * M + q;
-    a[q] = e < E ? rank_key(lg[e], e) : 0ull;
-  }
-  sort_desc<M>(a);
-  const int lanes = (E + M - 1) / M;
-  for (int s = 1; s < lanes || s < k; s <<= 1) keep_top_of_pair<M>(a, s);
+  for (int r = 0; r < R; ++r) a[r] = lane * R + r < n ? c[lane * R + r] : 0ull;
+  warp_sort_desc<R>(a);
   unsigned long long mine = 0ull;
 #pragma unroll
-  for (int q = 0; q < M; ++q)
-    if (q == lane) mine = a[q];
-  return mine;
-}
-
-// The same picks for k > 8 (E <= 256): k rounds of a warp-wide maximum of the
-// keys not yet taken (lane i holds experts i, i+32, ...), which needs fewer
-// registers than a 16-entry list. Lane j < k returns the key of pick j.
-__device__ __forceinline__ unsigned long long warp_topk_rounds(const float* lg, int E, int k) {
-  const int lane = threadIdx.x & 31;
-  unsigned long long v[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int e = lane + 32 * j;
-    v[j] = e < E ? rank_key(lg[e], e) : 0ull;
-  }
-  unsigned taken = 0u;
-  unsigned long long mine = 0ull;
-  for (int r = 0; r < k; ++r) {
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (!(taken >> j & 1u) && v[j] > best) best = v[j];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)best, o);
-      const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(best >> 32), o);
-      const unsigned long long b = ((unsigned long long)hi << 32) | lo;
-      best = b > best ? b : best;
-    }
-    const int e = key_expert(best);
-    if ((e & 31) == lane) taken |= 1u << (e >> 5);
-    if (r == lane) mine = best;
+  for (int r = 0; r < R; ++r) {
+    const unsigned long long x = __shfl_sync(0xffffffffu, a[r], lane / R);
+    if (lane % R == r) mine = x;
   }
   return mine;
 }
-
-// Top-k of every token of lg [T][E] (shared memory), one warp per token:
-// ids[t*k + j] (and vals, when given) receive pick j. Every thread calls it;
-// E <= 256, k <= 16.
-__device__ __forceinline__ void topk_rows_warps(const float* lg, int T, int E, int k, int* ids, float* vals) {
-  const int lane = threadIdx.x & 31;
-  const bool small = k <= 8;
-  for (int t = threadIdx.x >> 5; t < T; t += blockDim.x >> 5) {
-    const unsigned long long key = small ? warp_topk_row<8>(lg + t * E, E, k) : warp_topk_rounds(lg + t * E, E, k);
-    if (lane < k) {
-      ids[t * k + lane] = key_expert(key);
-      if (vals) vals[t * k + lane] = key_value(key);
-    }
-  }
+__device__ __forceinline__ unsigned long long topk_stage2(const unsigned long long* c, int n) {
+  if (n <= 32) return topk_stage2_r<1>(c, n);
+  if (n <= 64) return topk_stage2_r<2>(c, n);
+  return topk_stage2_r<4>(c, n);  // n <= 128: G <= 8 groups of K8 <= 16
 }
+
+__device__ __forceinline__ int topk_list_len(int k) { return k <= 8 ? 8 : 16; }
 
 template <int TC>
-__global__ void __launch_bounds__(kEnsureThreads, 1)
+__global__ void __launch_bounds__(kHeadThreads)
 route_ensure_cluster_kernel(RouteEnsureArgs a) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
@@ -464,25 +446,45 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   const RouteArgs& r = a.r;
   const unsigned crank = cluster.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = (int)crank * 32 + warp;
   const int H = r.H, E = r.E, T = r.T, k = r.k;
+  const int epc = (E + (int)cluster.num_blocks() - 1) / (int)cluster.num_blocks();  // experts per CTA
+  const int e0 = (int)crank * epc, e1 = min(E, e0 + epc);
   const bool pf = a.pf_n > 0;
   const int tc = T < TC ? T : TC;
   uint16_t* xs = reinterpret_cast<uint16_t*>(dyn);                  // [tc][H] bf16: this chunk's x
   int* ids_s = reinterpret_cast<int*>(xs + (size_t)tc * H);         // [T][k] routed ids (CTA 0)
   int* pid = ids_s + T * k;                                         // [T][k] predicted ids (CTA 1)
   int* cand = pid + T * k;                                          // [T][k] candidates (CTA 1)
+  uint16_t* rows_s = reinterpret_cast<uint16_t*>(                   // [epc][H] router rows (H <= kRowSmemH)
+      dyn + (((size_t)tc * H * 2 + (size_t)3 * T * k * 4 + 15) / 16));
   // Every CTA must have started before another writes into its shared memory:
   // arrive now, wait just before the first remote store.
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   if (crank == 0) ensure_load_table(sm, a.tab, E, a.S);
   if (pf && crank == 1) ensure_load_table(sm, a.tab_next, E, a.S);
-  const uint16_t* row = r.wr + (size_t)(e < E ? e : 0) * H;
-  const uint16_t* prow = pf ? a.wr_next + (size_t)(e < E ? e : 0) * H : row;
-  if (e < E) {
-    for (int c = lane * 64; c < H; c += 32 * 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + c));
-    if (pf)
-      for (int c = lane * 64; c < H; c += 32 * 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(prow + c));
+  // The router rows do not depend on the preceding kernel: with H <= kRowSmemH
+  // each warp copies its rows into shared memory (cp.async, 16 bytes per lane
+  // per step, each lane later reading only the chunks it copied) before the
+  // dependency wait, kept in L2 with the evict-last hint; longer rows, and the
+  // predictor's rows, are pulled into L2.
+  const bool row_in_smem = H <= kRowSmemH;
+  {
+    const unsigned long long keep = l2_evict_last();
+    for (int e = e0 + warp; e < e1; e += kHeadWarps) {
+      const uint16_t* row = r.wr + (size_t)e * H;
+      if (row_in_smem) {
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(rows_s + (size_t)(e - e0) * H);
+        for (int c = lane * 8; c < H; c += 256)
+          asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst + 2u * c),
+                       "l"(row + c), "l"(keep) : "memory");
+      } else {
+        for (int c = lane * 64; c < H; c += 32 * 64) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(row + c));
+      }
+      if (pf)
+        for (int c = lane * 64; c < H; c += 32 * 64)
+          asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(a.wr_next + (size_t)e * H + c));
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
   pdl_wait();
   pdl_trigger();
@@ -494,49 +496,61 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
     const int nt = min(TC, T - t0);
     // x rows of this chunk, read once per CTA into shared memory
     __syncthreads();
-    for (int i = threadIdx.x; i < nt * h8; i += kEnsureThreads)
+    for (int i = threadIdx.x; i < nt * h8; i += kHeadThreads)
       dyn[i] = __ldg(reinterpret_cast<const uint4*>(r.x + (size_t)t0 * H) + i);
+    if (t0 == 0) asm volatile("cp.async.wait_all;" ::: "memory");  // this lane's row chunks
     __syncthreads();
-    for (int pass = 0; pass < (pf ? 2 : 1) && e < E; ++pass) {
-      const uint16_t* wrow = pass ? prow : row;
-      float* dst = pass ? to1 : to0;
-      float acc[TC];
+    for (int e = e0 + warp; e < e1; e += kHeadWarps) {
+      const uint16_t* rs = rows_s + (size_t)(e - e0) * H;
+      for (int pass = 0; pass < (pf ? 2 : 1); ++pass) {
+        const uint16_t* wrow = (pass ? a.wr_next : r.wr) + (size_t)e * H;
+        float* dst = pass ? to1 : to0;
+        float acc[TC];
 #pragma unroll
-      for (int t = 0; t < TC; ++t) acc[t] = 0.0f;
-      for (int c0 = lane * 8; c0 < H; c0 += 256 * kRowUnroll) {
-        uint4 wv[kRowUnroll];
+        for (int t = 0; t < TC; ++t) acc[t] = 0.0f;
+        for (int c0 = lane * 8; c0 < H; c0 += 256 * kRowUnroll) {
+          uint4 wv[kRowUnroll];
+          if (pass == 0 && row_in_smem) {
 #pragma unroll
-        for (int u = 0; u < kRowUnroll; ++u) {
-          const int c = c0 + 256 * u;
-          wv[u] = c < H ? ld_stream(wrow + c) : make_uint4(0u, 0u, 0u, 0u);
-        }
+            for (int u = 0; u < kRowUnroll; ++u) {
+              const int c = c0 + 256 * u;
+              wv[u] = c < H ? *reinterpret_cast<const uint4*>(rs + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+          } else {
 #pragma unroll
-        for (int u = 0; u < kRowUnroll; ++u) {
-          const int c = c0 + 256 * u;
-          if (c < H) {
+            for (int u = 0; u < kRowUnroll; ++u) {
+              const int c = c0 + 256 * u;
+              wv[u] = c < H ? ld_keep(wrow + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
 #pragma unroll
-            for (int t = 0; t < TC; ++t) {
-              if (t < nt) {
-                const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * H + c);
-                const float xf[8] = {bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y),
-                                     bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w)};
-                acc[t] = dot8(wv[u], xf, acc[t]);
+          for (int u = 0; u < kRowUnroll; ++u) {
+            const int c = c0 + 256 * u;
+            if (c < H) {
+#pragma unroll
+              for (int t = 0; t < TC; ++t) {
+                if (t < nt) {
+                  const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)t * H + c);
+                  const float xf[8] = {bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y),
+                                       bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w)};
+                  acc[t] = dot8(wv[u], xf, acc[t]);
+                }
               }
             }
           }
         }
-      }
-      float sums[TC];
+        float sums[TC];
 #pragma unroll
-      for (int t = 0; t < TC; ++t) sums[t] = warp_sum(acc[t]);
-      if (!waited) {
-        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-        waited = true;
-      }
-      if (lane == 0) {
+        for (int t = 0; t < TC; ++t) sums[t] = warp_sum(acc[t]);
+        if (!waited) {
+          asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+          waited = true;
+        }
+        if (lane == 0) {
 #pragma unroll
-        for (int t = 0; t < TC; ++t)
-          if (t < nt) dst[(t0 + t) * E + e] = sums[t];
+          for (int t = 0; t < TC; ++t)
+            if (t < nt) dst[(t0 + t) * E + e] = sums[t];
+        }
       }
     }
   }
@@ -544,7 +558,13 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   cluster.sync();  // every logit is in CTA 0's (and predicted ones in CTA 1's) shared memory
   if (pf && crank == 1) {
     // Lookahead into the next layer: predicted top-k, candidates, install.
-    topk_rows_warps(lall, T, E, k, pid, nullptr);
+    const int K8 = topk_list_len(k), G = (E + 31) >> 5;
+    topk_stage1(lall, T, E, K8, sm.key);  // sm.key is free until the candidates are ordered
+    __syncthreads();
+    for (int t = warp; t < T; t += kHeadWarps) {
+      const unsigned long long key = topk_stage2(sm.key + t * G * K8, G * K8);
+      if (lane < k) pid[t * k + lane] = key_expert(key);
+    }
     __syncthreads();
     const int nc = lookahead_candidates_block(sm, pid, lall, T, k, E, cand);
     install_block(sm, a.tab_next, cand, nc, a.pf_n, E, a.S, a.pf_bytes, true);
@@ -552,12 +572,15 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   }
   if (crank != 0) return;
 
-  // Each token's top-k and weights in one warp; the picks go to the caller's ids
-  // and weights and, for the slot update, to shared memory.
-  const bool small = k <= 8;
-  for (int t = warp; t < T; t += kEnsureThreads / 32) {
+  // Top-k in two stages (sm.key holds the candidates until the slot update), then
+  // each token's weights in one warp; the picks go to the caller's ids and
+  // weights and, for the slot update, to shared memory.
+  const int K8 = topk_list_len(k), G = (E + 31) >> 5;
+  topk_stage1(lall, T, E, K8, sm.key);
+  __syncthreads();
+  for (int t = warp; t < T; t += kHeadWarps) {
     const float* row = lall + t * E;
-    const unsigned long long key = small ? warp_topk_row<8>(row, E, k) : warp_topk_rounds(row, E, k);
+    const unsigned long long key = topk_stage2(sm.key + t * G * K8, G * K8);
     const float v = key_value(key);
     const float lmax = __shfl_sync(0xffffffffu, v, 0);
     const float ej = lane < k ? expf(v - lmax) : 0.0f;
@@ -587,18 +610,23 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
 }  // namespace
 
 // Dynamic shared memory of the cluster head: x of one token chunk [TC][H] bf16,
-// then with the lookahead on predicted ids and candidates [T][k] each.
-constexpr int kHeadPredSmemMax = kTokChunk * 8192 * 2 + 3 * 1024 * 4;
+// routed ids, predicted ids and candidates [T][k] each (T*k <= kHeadThreads),
+// then (H <= kRowSmemH) the router rows of the CTA's experts [<= 32][H] bf16.
+constexpr int kHeadSmemWide = kTokChunk * 8192 * 2 + 3 * kHeadThreads * 4 + 16;  // H = 8192
+constexpr int kHeadSmemRows =
+    kTokChunk * kRowSmemH * 2 + 3 * kHeadThreads * 4 + 16 + kHeadMaxEpc * kRowSmemH * 2;  // H <= 2048
+constexpr int kHeadSmemAttr = kHeadSmemWide > kHeadSmemRows ? kHeadSmemWide : kHeadSmemRows;
+static_assert(kHeadSmemAttr + (int)sizeof(EnsureSmem) + kClusterMaxLogits * 4 <= 227 * 1024, "head shared memory");
 
 cudaError_t route_init_attributes() {
   cudaError_t e = cudaFuncSetAttribute(route_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemMax);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(route_ensure_cluster_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kHeadPredSmemMax);
+                             kHeadSmemAttr);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(route_ensure_cluster_kernel<kTokChunk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kHeadPredSmemMax);
+                             kHeadSmemAttr);
   return e;
 }
 
@@ -621,17 +649,22 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t st) {
 cudaError_t launch_route_ensure(const RouteEnsureArgs& a, cudaStream_t st) {
   if (a.r.T <= 0) return cudaSuccess;
   if (a.r.T > kRouteEnsureMaxT || a.r.E > kEnsureMax || a.S > kEnsureMax) return cudaErrorInvalidValue;
-  const int per_cta = kEnsureThreads / 32;
-  const int grid = (a.r.E + per_cta - 1) / per_cta;
   if (a.pf_n > 0 && a.r.T * a.r.k > kEnsureThreads) return cudaErrorInvalidValue;
-  if (grid <= kClusterMaxCtas && a.r.T * a.r.E <= kClusterMaxLogits) {
-    const int cgrid = a.pf_n > 0 ? max(grid, 2) : grid;  // CTA 1 runs the lookahead
+  const int T = a.r.T, E = a.r.E, k = a.r.k;
+  const int cand = T * ((E + 31) / 32) * (k <= 8 ? 8 : 16);  // two-stage top-k candidates
+  if (E <= kClusterMaxCtas * kHeadMaxEpc && T * E <= kClusterMaxLogits && T * k <= kHeadThreads &&
+      cand <= kEnsureMax) {
+    const int cgrid = a.pf_n > 0 ? max(head_ctas(E), 2) : head_ctas(E);  // CTA 1 runs the lookahead
+    if ((E + cgrid - 1) / cgrid > kHeadMaxEpc) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(cgrid);
-    cfg.blockDim = dim3(kEnsureThreads);
-    const int tc = a.r.T == 1 ? 1 : min(a.r.T, kTokChunk);
-    cfg.dynamicSmemBytes = (size_t)tc * a.r.H * 2 + (size_t)(a.r.T * a.r.k) * 4 +
-                           (a.pf_n > 0 ? (size_t)(2 * a.r.T * a.r.k) * 4 : 0);
+    cfg.blockDim = dim3(kHeadThreads);
+    const int tc = T == 1 ? 1 : min(T, kTokChunk);
+    const int epc = (E + cgrid - 1) / cgrid;
+    // x chunk, then the three [T][k] id arrays (all reserved, so the row area's
+    // offset is the one the kernel computes), then the CTA's router rows
+    cfg.dynamicSmemBytes = ((size_t)tc * a.r.H * 2 + (size_t)3 * T * k * 4 + 15) / 16 * 16 +
+                           (a.r.H <= kRowSmemH ? (size_t)epc * a.r.H * 2 : 0);
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -642,17 +675,19 @@ cudaError_t launch_route_ensure(const RouteEnsureArgs& a, cudaStream_t st) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 2 : 1;
-    if (a.r.T == 1) return cudaLaunchKernelEx(&cfg, route_ensure_cluster_kernel<1>, a);
+    if (T == 1) return cudaLaunchKernelEx(&cfg, route_ensure_cluster_kernel<1>, a);
     return cudaLaunchKernelEx(&cfg, route_ensure_cluster_kernel<kTokChunk>, a);
   }
+  const int per_cta = kEnsureThreads / 32;
+  const int grid = (E + per_cta - 1) / per_cta;
   RouteEnsureArgs b = a;
   b.pf_n = 0;  // this kernel has no predictor: the lookahead follows as two launches
-  cudaError_t e = a.r.T == 1
+  cudaError_t e = T == 1
                       ? launch_k(route_ensure_kernel<1>, dim3(grid), dim3(kEnsureThreads), 0, st, a.pdl != 0, b)
                       : launch_k(route_ensure_kernel<kTokChunk>, dim3(grid), dim3(kEnsureThreads), 0, st,
                                  a.pdl != 0, b);
   if (e != cudaSuccess || a.pf_n <= 0) return e;
-  return launch_lookahead(a.r.x, a.wr_next, a.r.T, a.r.E, a.r.H, a.r.k, a.tab_next, a.S, a.pf_n, a.pf_bytes,
+  return launch_lookahead(a.r.x, a.wr_next, T, E, a.r.H, k, a.tab_next, a.S, a.pf_n, a.pf_bytes,
                           a.pred_logits, a.pred_ids, a.pred_w, a.pred_done, st);
 }
 
