@@ -12,13 +12,21 @@
 // the end of its bucket are computed and discarded; every output row depends
 // only on its own input row, so the bucket order never changes a result.
 //
+// A CTA holds NB accumulators of 256 fp32 columns (NB = 2 when the column
+// blocks pair up: 512 TMEM columns), so that each x (or h) tile it streams
+// feeds NB column blocks and the tile is read from memory 1/NB as often. At
+// prefill sizes (about 128 rows per expert) the kernels are bound by the
+// weight bytes they stream, so the ring is made of small stages (K = 32,
+// 64-byte swizzle) to keep more bytes in flight per SM.
+//
 // Warp roles (4 warps): warp 0 allocates TMEM and, one lane, issues the TMA
-// loads of a 4-stage shared-memory ring; warp 1, one lane, issues
-// tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate) and commits each
-// stage back to the producer; all 4 warps read the accumulator with
-// tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = tile rows) for the
-// epilogue. Every wait is bounded: a wait that runs out sets a status bit and
-// the CTA drains its own copies (again bounded), frees TMEM and returns.
+// loads of a shared-memory ring (8 stages for NB = 1, 5 stages of NB weight
+// tiles for NB = 2, K = 32 each); warp 1, one lane, issues tcgen05.mma (M=128, N=256, K=16,
+// bf16 in, fp32 accumulate; NB per K step) and commits each stage back to the
+// producer; all 4 warps read the accumulators with tcgen05.ld (warp w owns
+// TMEM lanes 32w..32w+31 = tile rows) for the epilogue. Every wait is bounded:
+// a wait that runs out sets a status bit and the CTA drains its own copies
+// (again bounded), frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -31,14 +39,18 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;        // tile rows (pairs)
-constexpr int BN = 256;        // accumulator columns
-constexpr int BK = 64;         // K per stage: one 128-byte swizzle row of bf16
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;     // 16 KB
-constexpr int B_BYTES = BN * BK * 2;     // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-constexpr uint32_t kTmemCols = 256;
+constexpr int BN = 256;        // columns of one accumulator
+constexpr int BK = 32;         // K per stage: one 64-byte swizzle row of bf16
+constexpr int A_BYTES = BM * BK * 2;     // 8 KB
+constexpr int B_BYTES = BN * BK * 2;     // 16 KB per accumulator
+template <int NB>
+struct Ring {
+  static constexpr int kStages = NB == 1 ? 8 : 5;
+  static constexpr int kStageBytes = A_BYTES + NB * B_BYTES;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+  static constexpr uint32_t kTmemCols = 256u * NB;
+};
+static_assert(Ring<2>::kSmemBytes <= 227 * 1024 && Ring<1>::kSmemBytes <= 227 * 1024, "GEMM shared memory");
 constexpr uint32_t kWaitLimit = 1u << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -75,15 +87,15 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* tm, uint64_t* bar
       : "memory");
 }
 
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
-// groups 1024 bytes apart (the layout a SWIZZLE_128B TMA box of 64 bf16 columns writes).
+// Shared-memory matrix descriptor: K-major operand, 64-byte swizzle, 8-row
+// groups 512 bytes apart (the layout a SWIZZLE_64B TMA box of 32 bf16 columns writes).
 __device__ __forceinline__ uint64_t sdesc(const void* p) {
   const uint64_t a = smem_u32(p);
   uint64_t d = (a >> 4) & 0x3FFFull;        // start address
   d |= 1ull << 16;                          // leading byte offset (unused with this swizzle)
-  d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)(512 >> 4) << 32;          // stride byte offset: 8 rows x 64 B
   d |= 1ull << 46;                          // descriptor version
-  d |= 2ull << 61;                          // 128-byte swizzle
+  d |= 4ull << 61;                          // 64-byte swizzle
   return d;
 }
 
@@ -137,9 +149,14 @@ __device__ bool tile_of(const int32_t* counts, const int32_t* offsets, const int
 }
 
 // MODE 1: gate/up + SiLU epilogue into Hp. MODE 2: down projection into Y by pair.
-template <int MODE>
+// Column block j = blockIdx.y * NB + a of accumulator a: gate rows j*128.. and up
+// rows I + j*128.. (MODE 1), or output columns j*256.. (MODE 2).
+template <int MODE, int NB>
 __global__ void __launch_bounds__(128, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, TcGemmArgs p) {
+  constexpr int STAGES = Ring<NB>::kStages;
+  constexpr int STAGE_BYTES = Ring<NB>::kStageBytes;
+  constexpr uint32_t kTmemCols = Ring<NB>::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
@@ -185,15 +202,19 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         break;
       }
       uint8_t* a_dst = smem + s * STAGE_BYTES;
-      uint8_t* b_dst = a_dst + A_BYTES;
       mbar_expect_tx(&full[s], STAGE_BYTES);
       tma_load_2d(&tm_a, &full[s], a_dst, kb * BK, row0);
-      if (MODE == 1) {
-        const int gate_row = g * 2 * p.I + blockIdx.y * (BN / 2);
-        tma_load_2d(&tm_b, &full[s], b_dst, kb * BK, gate_row);
-        tma_load_2d(&tm_b, &full[s], b_dst + B_BYTES / 2, kb * BK, gate_row + p.I);
-      } else {
-        tma_load_2d(&tm_b, &full[s], b_dst, kb * BK, g * p.H + blockIdx.y * BN);
+#pragma unroll
+      for (int ac = 0; ac < NB; ++ac) {
+        uint8_t* b_dst = a_dst + A_BYTES + ac * B_BYTES;
+        const int j = blockIdx.y * NB + ac;  // column block of accumulator ac
+        if (MODE == 1) {
+          const int gate_row = g * 2 * p.I + j * (BN / 2);
+          tma_load_2d(&tm_b, &full[s], b_dst, kb * BK, gate_row);
+          tma_load_2d(&tm_b, &full[s], b_dst + B_BYTES / 2, kb * BK, gate_row + p.I);
+        } else {
+          tma_load_2d(&tm_b, &full[s], b_dst, kb * BK, g * p.H + j * BN);
+        }
       }
       issued = kb + 1;
     }
@@ -209,10 +230,12 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       }
       tc_fence_after();
       const uint8_t* a = smem + s * STAGE_BYTES;
-      const uint8_t* b = a + A_BYTES;
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk)
-        mma_bf16(tmem, sdesc(a + kk * 32), sdesc(b + kk * 32), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ac = 0; ac < NB; ++ac)
+          mma_bf16(tmem + (uint32_t)(ac * BN), sdesc(a + kk * 32), sdesc(a + A_BYTES + ac * B_BYTES + kk * 32), idesc,
+                   (kb > 0 || kk > 0) ? 1u : 0u);
       mma_commit(&empty[s]);
     }
     mma_commit(done);
@@ -227,9 +250,12 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   __syncthreads();
   if (!s_fail) {
     const int r = warp * 32 + lane;  // tile row = TMEM lane
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_base0 = tmem + ((uint32_t)(warp * 32) << 16);
+    for (int ac = 0; ac < NB; ++ac) {
+    const uint32_t lane_base = lane_base0 + (uint32_t)(ac * BN);
+    const int j = blockIdx.y * NB + ac;
     if (MODE == 1) {
-      const int col0 = blockIdx.y * (BN / 2);
+      const int col0 = j * (BN / 2);
       for (int c = 0; c < BN / 2; c += 32) {
         uint32_t gv[32], uv[32];
         tmem_ld32(lane_base + c, gv);
@@ -255,7 +281,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         }
       }
     } else {
-      const int col0 = blockIdx.y * BN;
+      const int col0 = j * BN;
       const int pair = r < rows ? p.perm[row0 + r] : 0;
       for (int c = 0; c < BN; c += 32) {
         uint32_t v[32];
@@ -269,6 +295,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
                                  __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
         }
       }
+    }
     }
   } else if (warp == 0 && lane == 0) {
     // Drain: wait (bounded) for every load this CTA issued before its memory goes away.
@@ -309,14 +336,14 @@ cudaError_t encoder() {
   return cudaSuccess;
 }
 
-// 2-D bf16 tensor map [rows, cols] (cols contiguous), box rows x 64 columns, 128-byte swizzle.
+// 2-D bf16 tensor map [rows, cols] (cols contiguous), box rows x 32 columns, 64-byte swizzle.
 cudaError_t make_map(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -328,9 +355,16 @@ bool tc_gemm_supported(int H, int I) { return H % BN == 0 && I % (BN / 2) == 0 &
 int tc_gemm_tile_rows() { return BM; }
 
 cudaError_t tc_gemm_init_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(tc_grouped_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_grouped_gemm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaSuccess;
+  for (cudaError_t r : {cudaFuncSetAttribute(tc_grouped_gemm<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Ring<1>::kSmemBytes),
+                        cudaFuncSetAttribute(tc_grouped_gemm<1, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Ring<2>::kSmemBytes),
+                        cudaFuncSetAttribute(tc_grouped_gemm<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Ring<1>::kSmemBytes),
+                        cudaFuncSetAttribute(tc_grouped_gemm<2, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Ring<2>::kSmemBytes)})
+    if (e == cudaSuccess) e = r;
   return e;
 }
 
@@ -357,11 +391,19 @@ cudaError_t launch_tc_prefill(const TcPrefillArgs& a, cudaStream_t st) {
   p.y = a.y;
   p.status = a.status;
   const int max_tiles = (Tk + BM - 1) / BM + a.G;
+  // two accumulators per CTA where the column blocks pair up (I/128 and H/256 even)
+  const int cb1 = a.I / (BN / 2), cb2 = a.H / BN;
   p.K = a.H;
-  tc_grouped_gemm<1><<<dim3(max_tiles, a.I / (BN / 2)), 128, SMEM_BYTES, st>>>(ta1, tb1, p);
+  if (cb1 % 2 == 0)
+    tc_grouped_gemm<1, 2><<<dim3(max_tiles, cb1 / 2), 128, Ring<2>::kSmemBytes, st>>>(ta1, tb1, p);
+  else
+    tc_grouped_gemm<1, 1><<<dim3(max_tiles, cb1), 128, Ring<1>::kSmemBytes, st>>>(ta1, tb1, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.K = a.I;
-  tc_grouped_gemm<2><<<dim3(max_tiles, a.H / BN), 128, SMEM_BYTES, st>>>(ta2, tb2, p);
+  if (cb2 % 2 == 0)
+    tc_grouped_gemm<2, 2><<<dim3(max_tiles, cb2 / 2), 128, Ring<2>::kSmemBytes, st>>>(ta2, tb2, p);
+  else
+    tc_grouped_gemm<2, 1><<<dim3(max_tiles, cb2), 128, Ring<1>::kSmemBytes, st>>>(ta2, tb2, p);
   return cudaGetLastError();
 }
 
