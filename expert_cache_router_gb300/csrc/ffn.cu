@@ -426,6 +426,7 @@ ffn_down_combine_kernel(FfnArgs a) {
   __shared__ int glead[kMaxPairs];    // first pair of each distinct slot, in pair order
   __shared__ unsigned char lead[kMaxPairs];  // 1: first pair of a hit slot, 2: of a missed expert
   __shared__ float s_w[kMaxPairs];    // routing weights of the call
+  __shared__ int s_src[kMaxPairs];    // host source of each pair (installed or spilled expert), else -1
   __shared__ int s_groups;
   __shared__ int s_last;              // early down: this CTA resets the counters at its end
   __shared__ int s_waited;            // early down: warps past their last wait
@@ -433,9 +434,22 @@ ffn_down_combine_kernel(FfnArgs a) {
   const int H = a.H, I = a.I, k = a.k;
   constexpr int CE = Fmt<FMT>::kElems, EB = Fmt<FMT>::kBytes;
   const ExpertSizes z = sizes_of<FMT>(a);
+  // The slot ids, weights and host sources come from the kernel two launches
+  // back (the head), which has completed: read them once, together, into
+  // shared memory. Early down reads only these before its per-group waits
+  // (every gate/up CTA started after the head completed).
+  for (int p = threadIdx.x; p < Tk; p += kThreads) {
+    sid[p] = __ldcg(a.slot_ids + p);
+    s_w[p] = __ldcg(a.w + p);
+    s_src[p] = a.pair_src ? __ldcg(a.pair_src + p) : -1;
+  }
+  if (threadIdx.x == 0) {
+    s_last = 0;
+    s_waited = 0;
+  }
+  __syncthreads();
   if (a.pdl) {
-    // The slot ids come from the kernel two launches back, which has completed:
-    // pull this CTA's W2 rows of every slot into L2 while the gate/up launch
+    // Pull this CTA's W2 rows of every slot into L2 while the gate/up launch
     // still runs. (Lines of slots it is still filling are refreshed in L2 by
     // its stores; L1 is not filled.)
     const int lpr = (I * EB + 127) / 128;  // 128-byte lines per W2 row
@@ -444,26 +458,15 @@ ffn_down_combine_kernel(FfnArgs a) {
     for (int i = threadIdx.x; i < Tk * rows * lpr; i += kThreads) {
       const int p = i / (rows * lpr), rem = i - p * (rows * lpr);
       const int r = rem / lpr, line = rem - r * lpr;
-      const int s = __ldcg(a.slot_ids + p);
+      const int s = sid[p];
       if (s >= 0 && s < a.S)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(a.lw.slot_w2 + (size_t)s * z.e2 +
                                                       ((size_t)(r0p + r) * I) * EB + line * 128));
     }
   }
-  // Early down reads only what the head wrote before this point (every gate/up
-  // CTA started after the head completed); gate/up results are waited for per group.
   if (!a.sync) pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int p = threadIdx.x; p < Tk; p += kThreads) {
-    sid[p] = __ldcg(a.slot_ids + p);
-    s_w[p] = __ldcg(a.w + p);
-  }
-  if (threadIdx.x == 0) {
-    s_last = 0;
-    s_waited = 0;
-  }
-  __syncthreads();
   for (int p = threadIdx.x; p < Tk; p += kThreads) {
     const int s = sid[p];
     int first = 1, nx = -1;
@@ -471,7 +474,7 @@ ffn_down_combine_kernel(FfnArgs a) {
       if (sid[q] == s) { first = 0; break; }
     for (int q = p + 1; q < Tk; ++q)
       if (sid[q] == s) { nx = q; break; }
-    lead[p] = (unsigned char)(first ? ((a.pair_src && __ldcg(a.pair_src + p) >= 0) ? 2 : 1) : 0);
+    lead[p] = (unsigned char)(first ? (s_src[p] >= 0 ? 2 : 1) : 0);
     nxt[p] = nx;
   }
   __syncthreads();
@@ -516,7 +519,7 @@ ffn_down_combine_kernel(FfnArgs a) {
         if (FMT) s2 = a.lw.slot_s2 + (size_t)s * z.f2;
         filled = a.copy_through && lead[p0] == 2;
       } else if (s >= a.S && a.pair_src) {  // spilled: read from host memory
-        const int e = __ldcg(a.pair_src + p0);
+        const int e = s_src[p0];
         if (e >= 0 && e < a.E) {
           w2 = a.lw.host_w2 + (size_t)e * z.e2;
           if (FMT) s2 = a.lw.host_s2 + (size_t)e * z.f2;
