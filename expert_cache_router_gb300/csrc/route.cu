@@ -337,9 +337,10 @@ __host__ __device__ inline int head_ctas(int E) {
 // key) pads. Two stages, so that no single warp runs a long dependent chain:
 // (1) one warp per (token, group of 32 experts) sorts the group's keys with a
 // bitonic network across its lanes and keeps the K8 largest (K8 = 8 for k <= 8,
-// else 16); (2) one warp per token sorts its groups' G*K8 candidates the same
-// way, and pick j is element j. The k largest keys of a row are among the K8
-// largest of their groups, so the picks are those of the one-stage rule.
+// else 16); (2) one warp per token ranks its groups' G*K8 candidates by
+// counting, and pick j is the candidate of rank j. The k largest keys of a row
+// are among the K8 largest of their groups, so the picks are those of the
+// one-stage rule.
 __device__ __forceinline__ unsigned long long rank_key(float v, int e) {
   if (v != v) v = -INFINITY;
   if (v == 0.0f) v = 0.0f;  // -0 ranks with +0
@@ -410,27 +411,21 @@ __device__ __forceinline__ void topk_stage1(const float* lg, int T, int E, int K
   }
 }
 
-// Stage 2 for one token: the warp sorts its n <= 32*R candidates c[0..n);
-// lane j returns the key of pick j.
-template <int R>
-__device__ __forceinline__ unsigned long long topk_stage2_r(const unsigned long long* c, int n) {
+// Stage 2 for one token: the warp ranks its n <= 128 candidates c[0..n) (shared
+// memory; real keys are distinct, padding keys rank below every real one) by
+// counting, for each, the candidates above it, and records the candidate of
+// rank j < k in pick[j] (shared scratch of k ints). Lane j < k returns the key
+// of pick j.
+__device__ __forceinline__ unsigned long long topk_stage2(const unsigned long long* c, int n, int k, int* pick) {
   const int lane = threadIdx.x & 31;
-  unsigned long long a[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) a[r] = lane * R + r < n ? c[lane * R + r] : 0ull;
-  warp_sort_desc<R>(a);
-  unsigned long long mine = 0ull;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const unsigned long long x = __shfl_sync(0xffffffffu, a[r], lane / R);
-    if (lane % R == r) mine = x;
+  for (int i = lane; i < n; i += 32) {
+    const unsigned long long ki = c[i];
+    int r = 0;
+    for (int j = 0; j < n; ++j) r += c[j] > ki;
+    if (r < k) pick[r] = i;
   }
-  return mine;
-}
-__device__ __forceinline__ unsigned long long topk_stage2(const unsigned long long* c, int n) {
-  if (n <= 32) return topk_stage2_r<1>(c, n);
-  if (n <= 64) return topk_stage2_r<2>(c, n);
-  return topk_stage2_r<4>(c, n);  // n <= 128: G <= 8 groups of K8 <= 16
+  __syncwarp();
+  return lane < k ? c[pick[lane]] : 0ull;
 }
 
 __device__ __forceinline__ int topk_list_len(int k) { return k <= 8 ? 8 : 16; }
@@ -562,7 +557,7 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
     topk_stage1(lall, T, E, K8, sm.key);  // sm.key is free until the candidates are ordered
     __syncthreads();
     for (int t = warp; t < T; t += kHeadWarps) {
-      const unsigned long long key = topk_stage2(sm.key + t * G * K8, G * K8);
+      const unsigned long long key = topk_stage2(sm.key + t * G * K8, G * K8, k, ids_s + t * k);
       if (lane < k) pid[t * k + lane] = key_expert(key);
     }
     __syncthreads();
@@ -580,7 +575,7 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   __syncthreads();
   for (int t = warp; t < T; t += kHeadWarps) {
     const float* row = lall + t * E;
-    const unsigned long long key = topk_stage2(sm.key + t * G * K8, G * K8);
+    const unsigned long long key = topk_stage2(sm.key + t * G * K8, G * K8, k, pid + t * k);  // pid: scratch here
     const float v = key_value(key);
     const float lmax = __shfl_sync(0xffffffffu, v, 0);
     const float ej = lane < k ? expf(v - lmax) : 0.0f;
