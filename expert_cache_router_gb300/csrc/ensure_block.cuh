@@ -78,6 +78,23 @@ struct EnsureSmem {
   unsigned s_bad;
 };
 
+// Rank of every free slot's key among sm.key[0..S) (distinct keys; used slots,
+// sm.used[s] set, are not ranked), recorded as sm.slot_by_rank[rank] = s for
+// ranks below limit. One warp per slot: each lane counts the smaller keys among
+// every 32nd slot, the warp adds the counts. Every thread calls it (no barrier).
+static __device__ __forceinline__ void rank_free_slots(EnsureSmem& sm, int S, int limit) {
+  const int lane = threadIdx.x & 31;
+  for (int s = threadIdx.x >> 5; s < S; s += blockDim.x >> 5) {
+    if (sm.used[s]) continue;  // the same for the whole warp
+    const unsigned long long k0 = sm.key[s];
+    int r = 0;
+    for (int s2 = lane; s2 < S; s2 += 32) r += (sm.key[s2] < k0);
+    r = __reduce_add_sync(0xffffffffu, r);
+    if (lane == 0 && r < limit) sm.slot_by_rank[r] = s;
+  }
+}
+
+
 // Copy the layer's table into shared memory (no barrier; call before ensure_block
 // with a __syncthreads in between).
 static __device__ __forceinline__ void ensure_load_table(EnsureSmem& sm, const LayerTables& tab, int E, int S) {
@@ -140,12 +157,7 @@ static __device__ void ensure_block(EnsureSmem& sm, LayerTables tab, const int32
                                      ((unsigned long long)sm.st[tid] << 10) | (unsigned long long)tid;
   }
   __syncthreads();
-  if (tid < S && !sm.used[tid]) {
-    const unsigned long long k0 = sm.key[tid];
-    int r = 0;
-    for (int s2 = 0; s2 < S; ++s2) r += (sm.key[s2] < k0);
-    sm.slot_by_rank[r] = tid;  // ranks of the free slots are 0..free_slots-1
-  }
+  rank_free_slots(sm, S, S);  // ranks of the free slots are 0..free_slots-1
   __syncthreads();
 
   // Install the first free_slots misses; spill the rest.
@@ -205,6 +217,139 @@ static __device__ void ensure_block(EnsureSmem& sm, LayerTables tab, const int32
     atomicAdd(&tab.stats[kStatBytesCopied], (unsigned long long)installs * expert_bytes);
     atomicAdd(&tab.stats[kStatPrefetchHits], (unsigned long long)sm.s_pf_hits);
     if (sm.s_bad) atomicOr(status, kDevBadExpertId);
+  }
+}
+
+// The same update by one warp, for calls of at most kEnsureWarpPairs pairs on
+// at most kEnsureWarpSlots slots: lane p holds pair p, the lowest lane of each
+// expert stands for it, and the block's barriers become warp votes. Hits,
+// misses (ranked by expert id), installs (the i-th smallest free key for the
+// i-th miss, taken one at a time by a warp-wide minimum) and spills follow the
+// rule above, so tables, slot ids, miss lists and counts are those of
+// ensure_block. Every lane of one warp calls it, after ensure_load_table and a
+// barrier; the rest of the CTA may leave.
+constexpr int kEnsureWarpPairs = 32;
+constexpr int kEnsureWarpSlots = 64;
+
+static __device__ __forceinline__ bool ensure_fits_warp(int Tk, int S) {
+  return Tk <= kEnsureWarpPairs && S <= kEnsureWarpSlots;
+}
+
+static __device__ __forceinline__ unsigned long long free_slot_key(const EnsureSmem& sm, int s) {
+  return ((unsigned long long)(sm.se[s] >= 0) << 42) | ((unsigned long long)sm.st[s] << 10) |
+         (unsigned long long)s;
+}
+
+static __device__ void ensure_warp(EnsureSmem& sm, LayerTables tab, const int32_t* ids, int Tk, int E, int S,
+                                   int32_t* slot_ids, uint32_t* status, unsigned long long expert_bytes) {
+  constexpr unsigned kAll = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const uint32_t clock = sm.clock0 + 1u;
+  if (lane < S) sm.used[lane] = 0;
+  if (lane + 32 < S) sm.used[lane + 32] = 0;
+  const int e = lane < Tk ? ids[lane] : -1;
+  const bool valid = lane < Tk && e >= 0 && e < E;
+  const bool bad = __any_sync(kAll, lane < Tk && !valid);
+  if (valid) atomicAdd(&tab.route_counts[e], 1ull);
+  // lanes of the same expert (invalid lanes each on their own)
+  const unsigned same = __match_any_sync(kAll, valid ? e : -1 - lane);
+  const int lead = __ffs(same) - 1;
+  const bool first = valid && lead == lane;
+  const int s0 = first ? sm.es[e] : -1;
+  const bool hit = first && s0 >= 0;
+  const bool miss = first && s0 < 0;
+  const bool pf_hit = hit && sm.st[s0] == 0u;  // first use of a prefetched slot
+  __syncwarp();
+  if (hit) {
+    sm.st[s0] = clock;
+    sm.used[s0] = 1;
+  }
+  const unsigned miss_mask = __ballot_sync(kAll, miss);
+  const int hits = __popc(__ballot_sync(kAll, hit));
+  const int pf_hits = __popc(__ballot_sync(kAll, pf_hit));
+  const int misses = __popc(miss_mask);
+  int miss_rank = 0;  // missed experts with a smaller id
+  for (unsigned m = miss_mask; m; m &= m - 1) {
+    const int eq = __shfl_sync(kAll, e, __ffs(m) - 1);
+    miss_rank += eq < e;
+  }
+  const int free_slots = sm.frozen ? 0 : S - hits;  // a static placement spills every miss
+  const int installs = misses < free_slots ? misses : free_slots;
+  __syncwarp();
+  if (installs > 0) {
+    unsigned long long k0 = (lane < S && !sm.used[lane]) ? free_slot_key(sm, lane) : ~0ull;
+    unsigned long long k1 = (lane + 32 < S && !sm.used[lane + 32]) ? free_slot_key(sm, lane + 32) : ~0ull;
+    for (int r = 0; r < installs; ++r) {
+      const unsigned long long mk = k0 < k1 ? k0 : k1;
+      const uint32_t hi = __reduce_min_sync(kAll, (uint32_t)(mk >> 32));
+      const uint32_t lo = __reduce_min_sync(kAll, (uint32_t)(mk >> 32) == hi ? (uint32_t)mk : ~0u);
+      const unsigned long long win = ((unsigned long long)hi << 32) | lo;
+      if (k0 == win) k0 = ~0ull;
+      if (k1 == win) k1 = ~0ull;
+      if (miss && miss_rank == r) {
+        const int v = (int)(lo & 1023u);
+        const int old = sm.se[v];
+        if (old >= 0) sm.es[old] = -1;
+        sm.se[v] = e;
+        sm.es[e] = v;
+        sm.st[v] = clock;
+        tab.miss_expert[r] = e;
+        tab.miss_slot[r] = v;
+      }
+      __syncwarp();
+    }
+  }
+  int marker = -1;
+  if (miss && miss_rank >= free_slots) {
+    marker = S + (miss_rank - free_slots);
+    tab.miss_expert[miss_rank] = e;
+    tab.miss_slot[miss_rank] = marker;
+  }
+  // Expert ids to slot ids (or spill markers), and the pairs read from host memory.
+  const int g_marker = __shfl_sync(kAll, marker, lead);
+  const int g_missed = __shfl_sync(kAll, (int)miss, lead);
+  __syncwarp();
+  if (lane < Tk) {
+    int s = -1, src = -1;
+    if (valid) {
+      s = sm.es[e];
+      if (s < 0) s = g_marker;
+      if (g_missed) src = e;
+    }
+    slot_ids[lane] = s;
+    tab.pair_src[lane] = src;
+  }
+  // Write the table back.
+  for (int i = lane; i < S; i += 32) {
+    tab.slot_expert[i] = sm.se[i];
+    tab.stamp[i] = sm.st[i];
+  }
+  for (int i = lane; i < E; i += 32) tab.expert_slot[i] = sm.es[i];
+  if (lane == 0) {
+    const int spills = misses - installs;
+    *tab.clock = clock;
+    tab.counts[kCntMiss] = misses;
+    tab.counts[kCntSpill] = spills;
+    tab.counts[kCntInstall] = installs;
+    tab.counts[kCntDistinct] = hits + misses;
+    atomicAdd(&tab.stats[kStatCalls], 1ull);
+    atomicAdd(&tab.stats[kStatHits], (unsigned long long)hits);
+    atomicAdd(&tab.stats[kStatMisses], (unsigned long long)misses);
+    atomicAdd(&tab.stats[kStatSpills], (unsigned long long)spills);
+    atomicAdd(&tab.stats[kStatBytesCopied], (unsigned long long)installs * expert_bytes);
+    atomicAdd(&tab.stats[kStatPrefetchHits], (unsigned long long)pf_hits);
+    if (bad) atomicOr(status, kDevBadExpertId);
+  }
+}
+
+// The update of one call by the whole CTA (every thread calls it): one warp when
+// the call fits ensure_warp, else ensure_block.
+static __device__ void ensure_call(EnsureSmem& sm, LayerTables tab, const int32_t* ids, int Tk, int E, int S,
+                                   int32_t* slot_ids, uint32_t* status, unsigned long long expert_bytes) {
+  if (ensure_fits_warp(Tk, S)) {
+    if (threadIdx.x < 32) ensure_warp(sm, tab, ids, Tk, E, S, slot_ids, status, expert_bytes);
+  } else {
+    ensure_block(sm, tab, ids, Tk, E, S, slot_ids, status, expert_bytes);
   }
 }
 
@@ -290,12 +435,7 @@ static __device__ void install_block(EnsureSmem& sm, LayerTables tab, const int*
   const int taken = __syncthreads_count(tid < S && sm.used[tid]);
   const int nopen = S - taken;
   const int ninst = ntodo < nopen ? ntodo : nopen;
-  if (tid < S && !sm.used[tid]) {
-    const unsigned long long k0 = sm.key[tid];
-    int r = 0;
-    for (int s2 = 0; s2 < S; ++s2) r += (sm.key[s2] < k0);
-    if (r < ninst) sm.slot_by_rank[r] = tid;
-  }
+  rank_free_slots(sm, S, ninst);
   __syncthreads();
   if (tid < ninst) {
     const int e = sm.spill_marker[tid];

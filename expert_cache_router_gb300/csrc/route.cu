@@ -288,7 +288,7 @@ route_ensure_kernel(RouteEnsureArgs a) {
     }
   }
   __syncthreads();
-  ensure_block(sm, a.tab, r.ids, T * r.k, E, a.S, a.slot_ids, a.status, a.expert_bytes);
+  ensure_call(sm, a.tab, r.ids, T * r.k, E, a.S, a.slot_ids, a.status, a.expert_bytes);
   if (threadIdx.x == 0) *r.done = 0u;
 }
 
@@ -334,13 +334,9 @@ __host__ __device__ inline int head_ctas(int E) {
 // 64-bit key whose unsigned order is that rule: the logit's bits mapped to an
 // order-preserving unsigned integer (NaN read as -inf, -0 as +0) in the high
 // word, the complement of the expert id in the low word; 0 (below every real
-// key) pads. Two stages, so that no single warp runs a long dependent chain:
-// (1) one warp per (token, group of 32 experts) sorts the group's keys with a
-// bitonic network across its lanes and keeps the K8 largest (K8 = 8 for k <= 8,
-// else 16); (2) one warp per token ranks its groups' G*K8 candidates by
-// counting, and pick j is the candidate of rank j. The k largest keys of a row
-// are among the K8 largest of their groups, so the picks are those of the
-// one-stage rule.
+// key) pads. One warp per token holds the row's keys in registers (up to eight
+// per lane) and takes the k largest one at a time: no block barrier and no
+// shared-memory round trip between the logits and the picks.
 __device__ __forceinline__ unsigned long long rank_key(float v, int e) {
   if (v != v) v = -INFINITY;
   if (v == 0.0f) v = 0.0f;  // -0 ranks with +0
@@ -354,81 +350,47 @@ __device__ __forceinline__ float key_value(unsigned long long key) {
 }
 __device__ __forceinline__ int key_expert(unsigned long long key) { return (int)(~(uint32_t)key); }
 
-__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
-  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
-  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
-  return ((unsigned long long)hi << 32) | lo;
-}
-
-// Bitonic sort, descending, of the 32*R keys one warp holds R per lane (element
-// lane*R + r): compare-exchanges within a lane for strides below R, across
-// lanes (xor of stride/R) above.
+// One token's row lg[0..E) (E <= 32*R), R keys per lane: k rounds of a
+// warp-wide maximum, each two 32-bit reductions (the high words; then the low
+// words of the keys whose high word is that maximum), after which the winning
+// key leaves its lane. Lane j < k returns the key of pick j, other lanes 0.
+// A short loop, not an unrolled network: this code runs once per call, and a
+// long straight-line sequence would be fetched cold every time.
 template <int R>
-__device__ __forceinline__ void warp_sort_desc(unsigned long long (&a)[R]) {
+__device__ __forceinline__ unsigned long long topk_warp(const float* lg, int E, int k) {
   const int lane = threadIdx.x & 31;
+  unsigned long long a[R];
 #pragma unroll
-  for (int size = 2; size <= 32 * R; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride < R) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int j = r ^ stride;
-          if (j > r) {
-            const bool desc = ((lane * R + r) & size) == 0;
-            const unsigned long long x = a[r], y = a[j];
-            const bool sw = desc ? (x < y) : (x > y);
-            a[r] = sw ? y : x;
-            a[j] = sw ? x : y;
-          }
-        }
-      } else {
-        const int ls = stride / R;
-        const bool lower = (lane & ls) == 0;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const unsigned long long b = shfl_xor_u64(a[r], ls);
-          const bool keep_max = (((lane * R + r) & size) == 0) == lower;
-          a[r] = keep_max ? (a[r] > b ? a[r] : b) : (a[r] < b ? a[r] : b);
-        }
-      }
-    }
+  for (int r = 0; r < R; ++r) {
+    const int e = r * 32 + lane;
+    a[r] = e < E ? rank_key(lg[e], e) : 0ull;
   }
+  unsigned long long mine = 0ull;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    unsigned long long m[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) m[r] = a[r];
+#pragma unroll
+    for (int w = 1; w < R; w <<= 1)
+#pragma unroll
+      for (int r = 0; r + w < R; r += 2 * w) m[r] = m[r + w] > m[r] ? m[r + w] : m[r];
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(m[0] >> 32));
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(m[0] >> 32) == hi ? (uint32_t)m[0] : 0u);
+    const unsigned long long win = ((unsigned long long)hi << 32) | lo;
+    if (lane == j) mine = win;
+#pragma unroll
+    for (int r = 0; r < R; ++r) a[r] = a[r] == win ? 0ull : a[r];
+  }
+  return mine;
 }
 
-// Stage 1: every (token, group) of lg [T][E] (shared memory), one warp each; the
-// group's K8 largest keys, descending, go to cand[(t*G + g)*K8 ..]. Every thread
-// calls it; the caller synchronises before stage 2.
-__device__ __forceinline__ void topk_stage1(const float* lg, int T, int E, int K8, unsigned long long* cand) {
-  const int lane = threadIdx.x & 31;
-  const int G = (E + 31) >> 5;
-  for (int q = threadIdx.x >> 5; q < T * G; q += blockDim.x >> 5) {
-    const int t = q / G, g = q - t * G;
-    const int e = g * 32 + lane;
-    unsigned long long a[1] = {e < E ? rank_key(lg[t * E + e], e) : 0ull};
-    warp_sort_desc<1>(a);
-    if (lane < K8) cand[q * K8 + lane] = a[0];
-  }
+__device__ __forceinline__ unsigned long long topk_row(const float* lg, int E, int k) {
+  if (E <= 32) return topk_warp<1>(lg, E, k);
+  if (E <= 64) return topk_warp<2>(lg, E, k);
+  if (E <= 128) return topk_warp<4>(lg, E, k);
+  return topk_warp<8>(lg, E, k);
 }
-
-// Stage 2 for one token: the warp ranks its n <= 128 candidates c[0..n) (shared
-// memory; real keys are distinct, padding keys rank below every real one) by
-// counting, for each, the candidates above it, and records the candidate of
-// rank j < k in pick[j] (shared scratch of k ints). Lane j < k returns the key
-// of pick j.
-__device__ __forceinline__ unsigned long long topk_stage2(const unsigned long long* c, int n, int k, int* pick) {
-  const int lane = threadIdx.x & 31;
-  for (int i = lane; i < n; i += 32) {
-    const unsigned long long ki = c[i];
-    int r = 0;
-    for (int j = 0; j < n; ++j) r += c[j] > ki;
-    if (r < k) pick[r] = i;
-  }
-  __syncwarp();
-  return lane < k ? c[pick[lane]] : 0ull;
-}
-
-__device__ __forceinline__ int topk_list_len(int k) { return k <= 8 ? 8 : 16; }
 
 template <int TC>
 __global__ void __launch_bounds__(kHeadThreads)
@@ -553,11 +515,8 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   cluster.sync();  // every logit is in CTA 0's (and predicted ones in CTA 1's) shared memory
   if (pf && crank == 1) {
     // Lookahead into the next layer: predicted top-k, candidates, install.
-    const int K8 = topk_list_len(k), G = (E + 31) >> 5;
-    topk_stage1(lall, T, E, K8, sm.key);  // sm.key is free until the candidates are ordered
-    __syncthreads();
     for (int t = warp; t < T; t += kHeadWarps) {
-      const unsigned long long key = topk_stage2(sm.key + t * G * K8, G * K8, k, ids_s + t * k);
+      const unsigned long long key = topk_row(lall + t * E, E, k);
       if (lane < k) pid[t * k + lane] = key_expert(key);
     }
     __syncthreads();
@@ -567,15 +526,11 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   }
   if (crank != 0) return;
 
-  // Top-k in two stages (sm.key holds the candidates until the slot update), then
-  // each token's weights in one warp; the picks go to the caller's ids and
-  // weights and, for the slot update, to shared memory.
-  const int K8 = topk_list_len(k), G = (E + 31) >> 5;
-  topk_stage1(lall, T, E, K8, sm.key);
-  __syncthreads();
+  // Top-k and weights of each token in one warp; the picks go to the caller's ids
+  // and weights and, for the slot update, to shared memory.
   for (int t = warp; t < T; t += kHeadWarps) {
     const float* row = lall + t * E;
-    const unsigned long long key = topk_stage2(sm.key + t * G * K8, G * K8, k, pid + t * k);  // pid: scratch here
+    const unsigned long long key = topk_row(row, E, k);
     const float v = key_value(key);
     const float lmax = __shfl_sync(0xffffffffu, v, 0);
     const float ej = lane < k ? expf(v - lmax) : 0.0f;
@@ -599,7 +554,7 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
     }
   }
   __syncthreads();
-  ensure_block(sm, a.tab, ids_s, T * k, E, a.S, a.slot_ids, a.status, a.expert_bytes);
+  ensure_call(sm, a.tab, ids_s, T * k, E, a.S, a.slot_ids, a.status, a.expert_bytes);
 }
 
 }  // namespace
@@ -646,9 +601,7 @@ cudaError_t launch_route_ensure(const RouteEnsureArgs& a, cudaStream_t st) {
   if (a.r.T > kRouteEnsureMaxT || a.r.E > kEnsureMax || a.S > kEnsureMax) return cudaErrorInvalidValue;
   if (a.pf_n > 0 && a.r.T * a.r.k > kEnsureThreads) return cudaErrorInvalidValue;
   const int T = a.r.T, E = a.r.E, k = a.r.k;
-  const int cand = T * ((E + 31) / 32) * (k <= 8 ? 8 : 16);  // two-stage top-k candidates
-  if (E <= kClusterMaxCtas * kHeadMaxEpc && T * E <= kClusterMaxLogits && T * k <= kHeadThreads &&
-      cand <= kEnsureMax) {
+  if (E <= kClusterMaxCtas * kHeadMaxEpc && T * E <= kClusterMaxLogits && T * k <= kHeadThreads) {
     const int cgrid = a.pf_n > 0 ? max(head_ctas(E), 2) : head_ctas(E);  // CTA 1 runs the lookahead
     if ((E + cgrid - 1) / cgrid > kHeadMaxEpc) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg{};

@@ -15,7 +15,7 @@ slot_ensure_kernel(LayerTables tab, const int32_t* __restrict__ ids, int Tk, int
   __shared__ EnsureSmem sm;
   ensure_load_table(sm, tab, E, S);
   __syncthreads();
-  ensure_block(sm, tab, ids, Tk, E, S, slot_ids, status, expert_bytes);
+  ensure_call(sm, tab, ids, Tk, E, S, slot_ids, status, expert_bytes);
 }
 
 // Consistency audit of one layer's table (and, when given, of the FFN's early-down
