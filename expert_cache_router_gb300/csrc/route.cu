@@ -322,9 +322,12 @@ constexpr int kHeadThreads = 1024;
 constexpr int kHeadWarps = kHeadThreads / 32;
 constexpr int kHeadMaxEpc = 32;  // experts per CTA of the cluster head
 
-// CTAs of the cluster head for E experts (up to eight, one warp per expert).
+// CTAs of the cluster head for E experts (up to eight, one warp per expert, at
+// least 16 experts per CTA). The router dot products are bound by shared-memory
+// bandwidth (each warp reads its router row and its own copy of x), so spreading
+// the experts over more CTAs shortens them.
 __host__ __device__ inline int head_ctas(int E) {
-  const int c = (E + 31) / 32;
+  const int c = (E + 15) / 16;
   return c < 1 ? 1 : (c > kClusterMaxCtas ? kClusterMaxCtas : c);
 }
 
