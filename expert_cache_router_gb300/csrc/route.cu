@@ -315,20 +315,24 @@ route_ensure_kernel(RouteEnsureArgs a) {
 // install_block). The two CTAs write different layers' tables. Dynamic shared
 // memory: x of one token chunk [TC][H] (read once per CTA), routed ids,
 // predicted ids and candidates [T][k] each, the CTA's router rows [32][H].
-constexpr int kClusterMaxCtas = 8;
 constexpr int kClusterMaxLogits = 2048;
+constexpr int kHeadMaxE = 256;   // experts of the cluster head (eight keys per lane in the top-k)
 constexpr int kRowSmemH = 2048;  // router rows staged in shared memory up to this hidden size
 constexpr int kHeadThreads = 1024;
 constexpr int kHeadWarps = kHeadThreads / 32;
 constexpr int kHeadMaxEpc = 32;  // experts per CTA of the cluster head
 
-// CTAs of the cluster head for E experts (up to eight, one warp per expert, at
-// least 16 experts per CTA). The router dot products are bound by shared-memory
-// bandwidth (each warp reads its router row and its own copy of x), so spreading
-// the experts over more CTAs shortens them.
-__host__ __device__ inline int head_ctas(int E) {
+// Largest cluster of the head: 16 CTAs (a non-portable size) where the device
+// can hold such a cluster of this kernel, else 8. Set by route_init_attributes.
+int g_head_cluster_max = 8;
+
+// CTAs of the cluster head for E experts (one warp per expert, at least 16
+// experts per CTA, up to g_head_cluster_max CTAs). The router dot products are
+// bound by shared-memory bandwidth (each warp reads its router row and its own
+// copy of x), so spreading the experts over more CTAs shortens them.
+inline int head_ctas(int E) {
   const int c = (E + 15) / 16;
-  return c < 1 ? 1 : (c > kClusterMaxCtas ? kClusterMaxCtas : c);
+  return c < 1 ? 1 : (c > g_head_cluster_max ? g_head_cluster_max : c);
 }
 
 // Top-k of rows [T][E] of logits in shared memory with the rule of
@@ -580,6 +584,29 @@ cudaError_t route_init_attributes() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(route_ensure_cluster_kernel<kTokChunk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kHeadSmemAttr);
+  if (e == cudaSuccess) {
+    // 16-CTA head clusters where the device holds one (both instantiations).
+    int fits = 1;
+    for (auto kern : {route_ensure_cluster_kernel<1>, route_ensure_cluster_kernel<kTokChunk>}) {
+      int n = 0;
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(16);
+      cfg.blockDim = dim3(kHeadThreads);
+      cfg.dynamicSmemBytes = kHeadSmemAttr;
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = 16;
+      at.val.clusterDim.y = 1;
+      at.val.clusterDim.z = 1;
+      cfg.attrs = &at;
+      cfg.numAttrs = 1;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+          cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1)
+        fits = 0;
+    }
+    (void)cudaGetLastError();  // a refused query leaves the portable size, not an error
+    g_head_cluster_max = fits ? 16 : 8;
+  }
   return e;
 }
 
@@ -604,7 +631,7 @@ cudaError_t launch_route_ensure(const RouteEnsureArgs& a, cudaStream_t st) {
   if (a.r.T > kRouteEnsureMaxT || a.r.E > kEnsureMax || a.S > kEnsureMax) return cudaErrorInvalidValue;
   if (a.pf_n > 0 && a.r.T * a.r.k > kEnsureThreads) return cudaErrorInvalidValue;
   const int T = a.r.T, E = a.r.E, k = a.r.k;
-  if (E <= kClusterMaxCtas * kHeadMaxEpc && T * E <= kClusterMaxLogits && T * k <= kHeadThreads) {
+  if (E <= kHeadMaxE && T * E <= kClusterMaxLogits && T * k <= kHeadThreads) {
     const int cgrid = a.pf_n > 0 ? max(head_ctas(E), 2) : head_ctas(E);  // CTA 1 runs the lookahead
     if ((E + cgrid - 1) / cgrid > kHeadMaxEpc) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg{};
