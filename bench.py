@@ -593,9 +593,11 @@ def summarize(cfg, store, r1, K, world, link, hbm_peak, traffic=None):
     return out
 
 
-def sub_workload(args, base, variants, K, W, dev, stream, dist, link, hbm_peak):
+def sub_workload(args, base, variants, K, W, dev, stream, dist, link, hbm_peak, cpu_seconds=0.0):
     """Another workload on the driver's clock: its own host store (freed afterwards), one
-    handle per variant (slot count or lookahead depth), SUB_REPEATS timed passes each."""
+    handle per variant (slot count or lookahead depth), SUB_REPEATS timed passes each; with
+    cpu_seconds > 0 (rank 0) also the oracle on the first tokens of the same stream, which
+    does not depend on the variant."""
     import numpy as np
     import torch
     store = Store(base, f"[rank {dist.rank}] ", allocator=pinned_allocator)
@@ -614,6 +616,11 @@ def sub_workload(args, base, variants, K, W, dev, stream, dist, link, hbm_peak):
                                   warmup=W, **summarize(cfg, store, r, K, dist.world, link, hbm_peak))
             finally:
                 moe.close()
+        if cpu_seconds > 0 and dist.rank == 0:
+            rate, ntok, cores, dt = cpu_oracle_rate(store, xt_host, cpu_seconds)
+            res["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                                   "sample": f"first {ntok} tokens of the timed stream at batch 1, all "
+                                             f"{base.num_layers} layers ({dt:.1f} s)"}
         return res
     finally:
         del store
@@ -754,10 +761,12 @@ def run_ours(args, dist):
         # over its own configured token count and seeded streams
         mx = MIXTRAL_8X7B
         line["mixtral"] = sub_workload(args, mx, [(f"S{S}", replace(mx, num_slots=S)) for S in (2, 4)],
-                                       mx.decode_tokens, max(W, 3), dev, stream, dist, link, hbm_peak)
+                                       mx.decode_tokens, max(W, 3), dev, stream, dist, link, hbm_peak,
+                                       cpu_seconds=min(args.cpu_seconds, 10.0))
         f8 = FP8_LOOKAHEAD
         line["fp8_lookahead"] = sub_workload(args, f8, [(f"N{N}", replace(f8, prefetch_n=N)) for N in (0, 1, 2, 4)],
-                                             f8.decode_tokens, max(W, 3), dev, stream, dist, link, hbm_peak)
+                                             f8.decode_tokens, max(W, 3), dev, stream, dist, link, hbm_peak,
+                                             cpu_seconds=min(args.cpu_seconds, 10.0))
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
 
