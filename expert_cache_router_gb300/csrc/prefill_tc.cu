@@ -149,7 +149,7 @@ __device__ bool tile_of(const int32_t* counts, const int32_t* offsets, const int
 }
 
 // MODE 1: gate/up + SiLU epilogue into Hp. MODE 2: down projection into Y by pair.
-// Column block j = blockIdx.y * NB + a of accumulator a: gate rows j*128.. and up
+// Column block j = blockIdx.x * NB + a of accumulator a: gate rows j*128.. and up
 // rows I + j*128.. (MODE 1), or output columns j*256.. (MODE 2).
 template <int MODE, int NB>
 __global__ void __launch_bounds__(128, 1)
@@ -165,8 +165,11 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   __shared__ int s_fail;
 
+  // blockIdx.x: column block pair, blockIdx.y: row tile. The CTAs of one tile are adjacent in
+  // launch order, so they run together and its x (or h) tile is read from DRAM once and then
+  // from L2; so are the tiles of one bucket, which share its weights.
   int g, row0, rows;
-  if (!tile_of(p.counts, p.offsets, p.tiles, p.G, blockIdx.x, &g, &row0, &rows)) return;
+  if (!tile_of(p.counts, p.offsets, p.tiles, p.G, blockIdx.y, &g, &row0, &rows)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = p.K / BK;
 
@@ -207,7 +210,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 #pragma unroll
       for (int ac = 0; ac < NB; ++ac) {
         uint8_t* b_dst = a_dst + A_BYTES + ac * B_BYTES;
-        const int j = blockIdx.y * NB + ac;  // column block of accumulator ac
+        const int j = blockIdx.x * NB + ac;  // column block of accumulator ac
         if (MODE == 1) {
           const int gate_row = g * 2 * p.I + j * (BN / 2);
           tma_load_2d(&tm_b, &full[s], b_dst, kb * BK, gate_row);
@@ -253,7 +256,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     const uint32_t lane_base0 = tmem + ((uint32_t)(warp * 32) << 16);
     for (int ac = 0; ac < NB; ++ac) {
     const uint32_t lane_base = lane_base0 + (uint32_t)(ac * BN);
-    const int j = blockIdx.y * NB + ac;
+    const int j = blockIdx.x * NB + ac;
     if (MODE == 1) {
       const int col0 = j * (BN / 2);
       for (int c = 0; c < BN / 2; c += 32) {
@@ -395,15 +398,15 @@ cudaError_t launch_tc_prefill(const TcPrefillArgs& a, cudaStream_t st) {
   const int cb1 = a.I / (BN / 2), cb2 = a.H / BN;
   p.K = a.H;
   if (cb1 % 2 == 0)
-    tc_grouped_gemm<1, 2><<<dim3(max_tiles, cb1 / 2), 128, Ring<2>::kSmemBytes, st>>>(ta1, tb1, p);
+    tc_grouped_gemm<1, 2><<<dim3(cb1 / 2, max_tiles), 128, Ring<2>::kSmemBytes, st>>>(ta1, tb1, p);
   else
-    tc_grouped_gemm<1, 1><<<dim3(max_tiles, cb1), 128, Ring<1>::kSmemBytes, st>>>(ta1, tb1, p);
+    tc_grouped_gemm<1, 1><<<dim3(cb1, max_tiles), 128, Ring<1>::kSmemBytes, st>>>(ta1, tb1, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.K = a.I;
   if (cb2 % 2 == 0)
-    tc_grouped_gemm<2, 2><<<dim3(max_tiles, cb2 / 2), 128, Ring<2>::kSmemBytes, st>>>(ta2, tb2, p);
+    tc_grouped_gemm<2, 2><<<dim3(cb2 / 2, max_tiles), 128, Ring<2>::kSmemBytes, st>>>(ta2, tb2, p);
   else
-    tc_grouped_gemm<2, 1><<<dim3(max_tiles, cb2), 128, Ring<1>::kSmemBytes, st>>>(ta2, tb2, p);
+    tc_grouped_gemm<2, 1><<<dim3(cb2, max_tiles), 128, Ring<1>::kSmemBytes, st>>>(ta2, tb2, p);
   return cudaGetLastError();
 }
 
