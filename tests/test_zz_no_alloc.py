@@ -151,3 +151,77 @@ def test_noalloc_flags_an_expert_id_outside_the_arrays(dev):
     rows = [0, 2, 3]
     want, _ = oracle.moe_ffn(hst["x"][rows], hst["ids"][rows], hst["w"][rows], hst["w13"], hst["w2"])
     assert_rows(oracle.bf16_to_f32(out.cpu().numpy().view(np.uint16))[rows], want)
+
+
+def test_noalloc_in_a_second_context_of_the_same_device(dev):
+    """A plug-in runtime may call the entry point under a driver context of its
+    own. In a second context on the same device (buffers allocated there, made
+    current on this thread), two calls give the bits of the call in the first
+    context: the scratch array's address is looked up in the current context on
+    every call, so a cached address from the other context is never used."""
+    import ctypes
+    from expert_cache_router_gb300 import grouped_ffn_noalloc, _lib as C
+    E, k, H, I, T = 8, 2, 256, 512, 5
+    hst, d = _noalloc_case(dev, E, k, H, I, T, seed=91)
+    ref = torch.zeros((T, H), dtype=torch.int16, device=dev)
+    grouped_ffn_noalloc(d["w13"], d["w2"], E, H, I, d["x"], d["ids"], d["w"], T, k, ref)
+    torch.cuda.synchronize()
+    ref = ref.cpu().numpy()
+
+    cu = ctypes.CDLL("libcuda.so.1")
+    u64, vp, sz = ctypes.c_uint64, ctypes.c_void_p, ctypes.c_size_t
+    for name, args in (("cuCtxGetCurrent", [ctypes.POINTER(vp)]),
+                       ("cuCtxSetCurrent", [vp]),
+                       ("cuCtxCreate_v2", [ctypes.POINTER(vp), ctypes.c_uint, ctypes.c_int]),
+                       ("cuCtxDestroy_v2", [vp]),
+                       ("cuCtxSynchronize", []),
+                       ("cuDeviceGet", [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+                       ("cuMemAlloc_v2", [ctypes.POINTER(u64), sz]),
+                       ("cuMemFree_v2", [u64]),
+                       ("cuMemsetD32_v2", [u64, ctypes.c_uint, sz]),
+                       ("cuMemcpyHtoD_v2", [u64, vp, sz]),
+                       ("cuMemcpyDtoH_v2", [vp, u64, sz])):
+        if not hasattr(cu, name):
+            pytest.skip(f"driver without {name}")
+        getattr(cu, name).argtypes = args
+        getattr(cu, name).restype = ctypes.c_int
+
+    def ck(r, what):
+        assert r == 0, f"{what}: CUresult {r}"
+
+    first = vp()
+    ck(cu.cuCtxGetCurrent(ctypes.byref(first)), "cuCtxGetCurrent")
+    cudev = ctypes.c_int()
+    ck(cu.cuDeviceGet(ctypes.byref(cudev), dev.index or 0), "cuDeviceGet")
+    ctx = vp()
+    ck(cu.cuCtxCreate_v2(ctypes.byref(ctx), 0, cudev), "cuCtxCreate")  # current on this thread now
+    bufs = []
+    try:
+        def put(a):
+            a = np.ascontiguousarray(a)
+            p = u64()
+            ck(cu.cuMemAlloc_v2(ctypes.byref(p), max(a.nbytes, 16)), "cuMemAlloc")
+            bufs.append(p.value)
+            ck(cu.cuMemcpyHtoD_v2(p.value, a.ctypes.data, a.nbytes), "cuMemcpyHtoD")
+            return p.value
+        w13, w2, x = put(hst["w13"].view(np.int16)), put(hst["w2"].view(np.int16)), put(hst["x"].view(np.int16))
+        ids, w = put(hst["ids"]), put(hst["w"])
+        out, status = put(np.zeros((T, H), np.int16)), put(np.zeros(4, np.uint32))
+        L = C.load()
+        for call in range(2):
+            ck(cu.cuMemsetD32_v2(out, 0x7FFF7FFF, T * H // 2), "cuMemsetD32")
+            st = L.moe_offload_grouped_ffn_noalloc(w13, w2, E, H, I, x, ids, w, T, k, out, status, None)
+            assert st == C.MOE_OK, L.moe_offload_last_error(None).decode()
+            ck(cu.cuCtxSynchronize(), "cuCtxSynchronize")
+            got = np.zeros((T, H), np.int16)
+            ck(cu.cuMemcpyDtoH_v2(got.ctypes.data, out, got.nbytes), "cuMemcpyDtoH")
+            sw = np.zeros(4, np.uint32)
+            ck(cu.cuMemcpyDtoH_v2(sw.ctypes.data, status, sw.nbytes), "cuMemcpyDtoH")
+            assert np.array_equal(got, ref), f"call {call} in the second context"
+            assert int(sw[0]) == 0
+    finally:
+        for p in bufs:
+            cu.cuMemFree_v2(p)
+        cu.cuCtxDestroy_v2(ctx)
+        cu.cuCtxSetCurrent(first)
+    torch.cuda.synchronize()  # the first context still works
