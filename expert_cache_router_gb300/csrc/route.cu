@@ -293,16 +293,18 @@ route_ensure_kernel(RouteEnsureArgs a) {
 }
 
 // Cluster variant of the fused head (E <= 256, T*E <= kClusterMaxLogits, T*k <=
-// kHeadThreads): one thread-block cluster of up to eight CTAs, each owning a
-// contiguous range of at most 32 experts, one warp per expert. Each warp copies
+// kHeadThreads): one thread-block cluster of up to 8 CTAs (16 where the device
+// holds such a cluster), each owning a contiguous range of at least 16 and at
+// most 32 experts, one warp per expert. Each warp copies
 // its router row into shared memory (cp.async) before the dependency wait, so
 // that once x is in the dot products read only shared memory (a CTA of this
 // size cannot become resident beside the preceding kernel's CTAs, so the copy
 // overlaps at least the launch and the wait). Each warp stores its logits
 // straight into CTA 0's shared memory (distributed shared memory: no global
 // round trip, fence or counter);
-// after one cluster barrier CTA 0 takes each token's top-k and updates the slot
-// table while the other CTAs exit. Same picks, weights and table as the other
+// after one cluster barrier CTA 0 takes each token's top-k (one warp per token)
+// and updates the slot table (one warp for calls of up to 32 pairs on up to 64
+// slots) while the other CTAs exit. Same picks, weights and table as the other
 // head kernels.
 //
 // With the router lookahead on (a.pf_n > 0, at least two CTAs), each warp also
