@@ -14,6 +14,11 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CUDA", 3: "MOE_ER
                 4: "MOE_ERR_CAPTURE", 5: "MOE_ERR_DEVICE_STATUS"}
 MOE_DTYPE_BF16, MOE_DTYPE_FP8_E4M3_B128 = 0, 1
 MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_SLOT_ID, MOE_DEV_AUDIT_FAILED, MOE_DEV_BAD_COUNT, MOE_DEV_TIMEOUT = 1, 2, 4, 8, 16
+MOE_TRACE_FIELDS = 16
+# decode trace record fields (moe_offload_trace_read), in order
+TRACE_FIELD_NAMES = ("head_wait", "head_logits", "head_topk", "head_done", "gate_first", "host_first",
+                     "host_done", "copy_done", "gate_done", "down_first", "down_waits", "down_done")
+TRACE_MIN_FIELDS = ("gate_first", "host_first", "down_first")
 
 # Every symbol the header declares, in declaration order.
 EXPORTS = [
@@ -26,7 +31,8 @@ EXPORTS = [
     "moe_offload_read_slot_scales", "moe_offload_set_shared_expert", "moe_offload_reset",
     "moe_offload_host_alloc", "moe_offload_host_free", "moe_offload_prefill_times",
     "moe_offload_device_bytes", "moe_offload_get_config", "moe_offload_read_routing",
-    "moe_offload_host_read_gbs", "moe_offload_debug_wait", "moe_offload_graph_create", "moe_offload_graph_launch",
+    "moe_offload_host_read_gbs", "moe_offload_debug_wait", "moe_offload_trace_enable", "moe_offload_trace_read",
+    "moe_offload_graph_create", "moe_offload_graph_launch",
     "moe_offload_graph_launch_host", "moe_offload_graph_times", "moe_offload_graph_kernel_count",
     "moe_offload_graph_destroy", "moe_offload_grouped_ffn_noalloc", "moe_offload_last_error",
     "moe_offload_destroy",
@@ -126,6 +132,10 @@ def _declare(L):
                                             ctypes.POINTER(ctypes.c_double)]
     L.moe_offload_debug_wait.restype = _st
     L.moe_offload_debug_wait.argtypes = [_vp, ctypes.c_longlong, ctypes.c_int]
+    L.moe_offload_trace_enable.restype = _st
+    L.moe_offload_trace_enable.argtypes = [_vp, ctypes.c_int]
+    L.moe_offload_trace_read.restype = _st
+    L.moe_offload_trace_read.argtypes = [_vp, _vp, ctypes.c_int]
     L.moe_offload_graph_create.restype = _st
     L.moe_offload_graph_create.argtypes = [_vp, ctypes.c_int, _vp, _vp, ctypes.c_int, ctypes.POINTER(_vp)]
     L.moe_offload_graph_launch.restype = _st

@@ -324,6 +324,18 @@ class MoeOffload:
         that makes the first group's wait of every down warp run out."""
         self._check(self._L.moe_offload_debug_wait(self.h, int(limit_ns), int(bool(stall))))
 
+    def trace_enable(self, on: bool = True) -> None:
+        """Decode trace on (records allocated and reset) or off, for launches enqueued
+        afterwards; decode graphs keep the setting they were created with."""
+        self._check(self._L.moe_offload_trace_enable(self.h, int(bool(on))))
+
+    def trace_read(self, reset: bool = True) -> np.ndarray:
+        """The decode trace records, [num_layers, MOE_TRACE_FIELDS] uint64 globaltimer
+        stamps (field names in _lib.TRACE_FIELD_NAMES); synchronises the device."""
+        out = np.zeros((self.num_layers, C.MOE_TRACE_FIELDS), np.uint64)
+        self._check(self._L.moe_offload_trace_read(self.h, out.ctypes.data, int(bool(reset))))
+        return out
+
     def prefill_times(self) -> dict:
         """Phase times (ms) of the last prefill call: route, copy, gemm, combine, staged."""
         v = [ctypes.c_float() for _ in range(4)]

@@ -50,6 +50,8 @@ struct moe_offload {
   int pdl = 1;  // programmatic dependent launch in the decode chain (env MOE_OFFLOAD_PDL=0 turns it off)
   int audit_each = 0;  // env MOE_OFFLOAD_AUDIT=1: audit a layer's table after every update of it
   int early_down = 1;  // env MOE_OFFLOAD_EARLY_DOWN=0: the down launch waits for the whole gate/up grid
+  unsigned long long* trace = nullptr;  // [L, kTraceFields] decode trace records (moe_offload_trace_enable)
+  int trace_on = 0;
   uint32_t* ffn_sync = nullptr;  // [kFfnSyncWords] counters of the early-down hand-off
   int last_tk = 0;               // T * k of the last decode-path call (ids_buf, w_buf, slot_buf)
   // Bound of the early-down waits, and the debug stall that plants a target no
@@ -284,6 +286,7 @@ FfnArgs ffn_args(moe_offload* h, int layer, const void* x, const int32_t* slot_i
   a.pair_src = h->tab[layer].pair_src;
   a.wait_ns = h->wait_ns;
   a.stall = h->stall;
+  a.tr = h->trace_on ? h->trace + (size_t)layer * kTraceFields : nullptr;
   return a;
 }
 
@@ -348,6 +351,7 @@ moe_status_t do_decode_head(moe_offload* h, int layer, const void* x, int T, cud
   a.status = h->status;
   a.expert_bytes = slot_bytes(h);
   a.pdl = (pdl && h->pdl) ? 1 : 0;
+  a.tr = h->trace_on ? h->trace + (size_t)layer * kTraceFields : nullptr;
   const bool pf = h->cfg.prefetch_n > 0 && layer + 1 < h->cfg.num_layers;
   if (pf) {
     // a copy into the next layer still in flight must finish before its slots change hands
@@ -1244,6 +1248,49 @@ moe_status_t moe_offload_debug_wait(moe_offload_t h, long long limit_ns, int sta
   h->wait_ns = limit_ns ? (unsigned long long)limit_ns : kDefaultWaitNs;
   h->stall = stall;
   return MOE_OK;
+}
+
+}  // extern "C"
+
+namespace {
+// The records' unset values: ~0 for the fields stamped with a minimum, 0 for the others.
+moe_status_t trace_reset(moe_offload* h) {
+  static_assert(MOE_TRACE_FIELDS == kTraceFields, "trace record size");
+  std::vector<unsigned long long> v((size_t)h->cfg.num_layers * kTraceFields, 0ull);
+  for (size_t i = 0; i < v.size(); ++i)
+    if (kTraceMinFields & (1u << (i % kTraceFields))) v[i] = ~0ull;
+  CK(h, cudaMemcpy(h->trace, v.data(), v.size() * sizeof(v[0]), cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_offload_trace_enable(moe_offload_t h, int on) {
+  if (!h) return MOE_ERR_INVALID;
+  if (on != 0 && on != 1) return fail(h, MOE_ERR_INVALID, "trace_enable: on=%d", on);
+  moe_status_t st = set_device(h);
+  if (st != MOE_OK) return st;
+  if (on) {
+    if (!h->trace &&
+        (st = dev_alloc(h, &h->trace, sizeof(unsigned long long) * (size_t)h->cfg.num_layers * kTraceFields)) !=
+            MOE_OK)
+      return st;
+    if ((st = trace_reset(h)) != MOE_OK) return st;
+  }
+  h->trace_on = on;
+  return MOE_OK;
+}
+
+moe_status_t moe_offload_trace_read(moe_offload_t h, uint64_t* out, int reset) {
+  if (!h || !out) return MOE_ERR_INVALID;
+  if (!h->trace) return fail(h, MOE_ERR_INVALID, "trace_read: the trace was never enabled");
+  moe_status_t st = set_device(h);
+  if (st != MOE_OK) return st;
+  CK(h, cudaDeviceSynchronize());
+  CK(h, cudaMemcpy(out, h->trace, sizeof(uint64_t) * (size_t)h->cfg.num_layers * kTraceFields,
+                   cudaMemcpyDeviceToHost));
+  return reset ? trace_reset(h) : MOE_OK;
 }
 
 const char* moe_offload_last_error(moe_offload_t h) {

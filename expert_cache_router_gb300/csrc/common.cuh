@@ -127,6 +127,34 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// Decode trace (moe_offload_trace_enable): per layer, kTraceFields globaltimer
+// stamps, each the earliest (trace_min) or latest (trace_max) time a kernel
+// passed a point of the step. tr == nullptr: off. Fire-and-forget atomics.
+enum TraceField {
+  kTrHeadWait = 0,      // head, CTA 0 past its dependency wait
+  kTrHeadLogits,        // head, every logit in CTA 0 (after the cluster barrier)
+  kTrHeadTopk,          // head, top-k and weights written
+  kTrHeadDone,          // head, slot table updated
+  kTrGateFirst,         // gate/up, first CTA past its dependency wait        (min)
+  kTrGateHostFirst,     // gate/up, first W2 bytes of an installed expert in   (min)
+  kTrGateHostDone,      // gate/up, last CTA of an installed expert done      (max)
+  kTrCopyDone,          // gate/up, last W2-copy CTA done                     (max)
+  kTrGateDone,          // gate/up, last CTA done                             (max)
+  kTrDownFirst,         // down, first CTA started                            (min)
+  kTrDownWaits,         // down, last CTA past its waits                      (max)
+  kTrDownDone,          // down, last CTA done                                (max)
+  kTraceFields = 16
+};
+constexpr unsigned kTraceMinFields =
+    (1u << kTrGateFirst) | (1u << kTrGateHostFirst) | (1u << kTrDownFirst);  // reset to ~0
+
+__device__ __forceinline__ void trace_min(unsigned long long* tr, int f) {
+  if (tr) atomicMin(tr + f, globaltimer_ns());
+}
+__device__ __forceinline__ void trace_max(unsigned long long* tr, int f) {
+  if (tr) atomicMax(tr + f, globaltimer_ns());
+}
+
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

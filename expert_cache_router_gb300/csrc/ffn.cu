@@ -242,7 +242,7 @@ __device__ void form_group(const FfnArgs& a, int* sid, int* members, Group* g, b
 
 // Copy-through workers: W2 (and FP8 scales) of every expert installed by this call, host -> slot.
 template <int FMT>
-__device__ void copy_installed_rest(const FfnArgs& a, int worker, int workers) {
+__device__ void copy_installed_rest(const FfnArgs& a, int worker, int workers, unsigned long long* tr) {
   const int n = min(__ldcg(a.counts + kCntInstall), a.S);
   if (n <= 0) return;
   const ExpertSizes z = sizes_of<FMT>(a);
@@ -284,25 +284,33 @@ __device__ void copy_installed_rest(const FfnArgs& a, int worker, int workers) {
 #pragma unroll
     for (int q = 0; q < U; ++q)
       if (d[q]) *d[q] = v[q];
+    if (u0 == t0 && threadIdx.x == 0) trace_min(tr, kTrGateHostFirst);  // first host bytes arrived
   }
 }
 
 // One token (TC = 1): four CTAs per SM (64 registers), so that the batch-1 grid of
 // 8 pairs + 4 copy columns x 48 row blocks is resident at once and the missed
 // expert's row blocks all start with the launch.
-template <int FMT, int TC>
+// TR: the decode-trace variant (stamps into a.tr); the plain one has none.
+template <int FMT, int TC, bool TR>
 __global__ void __launch_bounds__(kThreads, TC == 1 ? 4 : 0)
 ffn_gate_up_kernel(FfnArgs a) {
   __shared__ int sid[kMaxPairs];
   __shared__ int members[kMaxPairs];
   __shared__ Group g;
+  unsigned long long* const tr = TR ? a.tr : nullptr;
   pdl_wait();
   pdl_trigger();
+  if (threadIdx.x == 0) trace_min(tr, kTrGateFirst);
   const int Tk = a.T * a.k;
   const int cols = Tk + (a.shared ? 1 : 0);
   if ((int)blockIdx.x >= cols) {  // copy-through W2 workers
-    copy_installed_rest<FMT>(a, (blockIdx.x - cols) * gridDim.y + blockIdx.y, (gridDim.x - cols) * gridDim.y);
+    copy_installed_rest<FMT>(a, (blockIdx.x - cols) * gridDim.y + blockIdx.y, (gridDim.x - cols) * gridDim.y, tr);
     signal_done(a.sync, kSyncCopy);
+    if (threadIdx.x == 0) {
+      trace_max(tr, kTrCopyDone);
+      trace_max(tr, kTrGateDone);
+    }
     return;
   }
   if ((int)blockIdx.x < Tk) {
@@ -410,6 +418,10 @@ ffn_gate_up_kernel(FfnArgs a) {
     }
   }
   signal_done(a.sync, col_word);
+  if (threadIdx.x == 0) {
+    if (g.w13_dst) trace_max(tr, kTrGateHostDone);
+    trace_max(tr, kTrGateDone);
+  }
 }
 
 // Down projection + combine. CTA b owns output rows [8b, 8b+8) for every
@@ -417,9 +429,10 @@ ffn_gate_up_kernel(FfnArgs a) {
 // expert) and dot each of the 8 W2 rows with h of every pair routed to that
 // slot; the CTA then sums the k ranks of each token in rank order (and the
 // shared expert last, weight 1). No other CTA touches these rows.
-template <int FMT, int TC>
+template <int FMT, int TC, bool TR>
 __global__ void __launch_bounds__(kThreads)
 ffn_down_combine_kernel(FfnArgs a) {
+  unsigned long long* const tr = TR ? a.tr : nullptr;
   extern __shared__ float ys[];       // [Tk (+T)][kDownRowsPerCta]
   __shared__ int sid[kMaxPairs];
   __shared__ int nxt[kMaxPairs];      // next pair routed to the same slot, -1 at the end
@@ -434,6 +447,7 @@ ffn_down_combine_kernel(FfnArgs a) {
   const int H = a.H, I = a.I, k = a.k;
   constexpr int CE = Fmt<FMT>::kElems, EB = Fmt<FMT>::kBytes;
   const ExpertSizes z = sizes_of<FMT>(a);
+  if (threadIdx.x == 0) trace_min(tr, kTrDownFirst);
   // The slot ids, weights and host sources come from the kernel two launches
   // back (the head), which has completed: read them once, together, into
   // shared memory. Early down reads only these before its per-group waits
@@ -502,8 +516,10 @@ ffn_down_combine_kernel(FfnArgs a) {
   // wait, so that round trip overlaps the compute; the CTA that counts last
   // resets the counters at its end.
   auto waits_done = [&]() {
-    if (a.sync && lane == 0 && atomicAdd(&s_waited, 1) == kWarps - 1)
+    if (a.sync && lane == 0 && atomicAdd(&s_waited, 1) == kWarps - 1) {
       s_last = atomicAdd(a.sync + kSyncDone, 1u) == gridDim.x - 1;
+      trace_max(tr, kTrDownWaits);
+    }
   };
   if (warp >= ngroups) waits_done();
   for (int d = warp; d < ngroups; d += kWarps) {
@@ -634,6 +650,7 @@ ffn_down_combine_kernel(FfnArgs a) {
       }
     }
   }
+  if (threadIdx.x == 0) trace_max(tr, kTrDownDone);
 }
 
 template <int FMT, int TC>
@@ -642,19 +659,22 @@ cudaError_t launch_tc(const FfnArgs& a, int phase, cudaStream_t st) {
   if (phase == 0) {
     dim3 g1(Tk + (a.shared ? 1 : 0) + (a.copy_through ? kCopyCols : 0),
             (a.I + kGateRowsPerCta - 1) / kGateRowsPerCta);
-    return launch_k(ffn_gate_up_kernel<FMT, TC>, g1, dim3(kThreads), 0, st, a.pdl != 0, a);
+    if (TC == 1 && a.tr) return launch_k(ffn_gate_up_kernel<FMT, 1, true>, g1, dim3(kThreads), 0, st, a.pdl != 0, a);
+    return launch_k(ffn_gate_up_kernel<FMT, TC, false>, g1, dim3(kThreads), 0, st, a.pdl != 0, a);
   }
   const size_t smem = (size_t)(Tk + (a.shared ? a.T : 0)) * kDownRowsPerCta * sizeof(float);
-  return launch_k(ffn_down_combine_kernel<FMT, TC>, dim3((a.H + kDownRowsPerCta - 1) / kDownRowsPerCta),
-                  dim3(kThreads), smem, st, a.pdl != 0, a);
+  const dim3 g2((a.H + kDownRowsPerCta - 1) / kDownRowsPerCta);
+  if (TC == 1 && a.tr)
+    return launch_k(ffn_down_combine_kernel<FMT, 1, true>, g2, dim3(kThreads), smem, st, a.pdl != 0, a);
+  return launch_k(ffn_down_combine_kernel<FMT, TC, false>, g2, dim3(kThreads), smem, st, a.pdl != 0, a);
 }
 
 // Largest dynamic shared memory of a down launch: ys of kMaxPairs pairs.
 constexpr int kDownSmemMax = kMaxPairs * kDownRowsPerCta * (int)sizeof(float);
 
-template <int FMT, int TC>
+template <int FMT, int TC, bool TR = false>
 cudaError_t down_attr() {
-  return cudaFuncSetAttribute(ffn_down_combine_kernel<FMT, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(ffn_down_combine_kernel<FMT, TC, TR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kDownSmemMax);
 }
 
@@ -671,7 +691,8 @@ cudaError_t launch_fmt(const FfnArgs& a, int phase, cudaStream_t st) {
 cudaError_t ffn_init_attributes() {
   cudaError_t e = cudaSuccess;
   for (cudaError_t r : {down_attr<0, 1>(), down_attr<0, 2>(), down_attr<0, 4>(), down_attr<0, 8>(),
-                        down_attr<1, 1>(), down_attr<1, 2>(), down_attr<1, 4>(), down_attr<1, 8>()})
+                        down_attr<1, 1>(), down_attr<1, 2>(), down_attr<1, 4>(), down_attr<1, 8>(),
+                        down_attr<0, 1, true>(), down_attr<1, 1, true>()})
     if (e == cudaSuccess) e = r;
   return e;
 }

@@ -66,6 +66,7 @@ struct RouteEnsureArgs {
   int32_t* pred_ids;            // [T,k]
   float* pred_w;                // [T,k]
   unsigned* pred_done;          // [1], zero between calls
+  unsigned long long* tr;       // decode trace of this layer ([kTraceFields]) or nullptr
 };
 cudaError_t launch_route_ensure(const RouteEnsureArgs& a, cudaStream_t st);
 // Router lookahead as its own launches: the next layer's router on x (logits and
@@ -126,6 +127,7 @@ struct FfnArgs {
   int shared;               // 1: add the shared expert (lw.sh_*) to every token, weight 1, after the k ranks
   uint32_t* sync;           // early down: [kFfnSyncWords] zeroed counters, or nullptr (down waits for
                             // the whole gate/up grid)
+  unsigned long long* tr;    // decode trace of this layer ([kTraceFields]) or nullptr
   unsigned long long wait_ns;  // bound of one early-down wait (0: kDefaultWaitNs)
   int stall;                // debug: the first group's wait of every down warp targets one CTA more
                             // than its column has, so it runs out (tests of the bounded wait)

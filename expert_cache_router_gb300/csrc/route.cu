@@ -401,9 +401,11 @@ __device__ __forceinline__ unsigned long long topk_row(const float* lg, int E, i
   return topk_warp<8>(lg, E, k);
 }
 
-template <int TC>
+// TR: the decode-trace variant (stamps into a.tr); the plain one has none.
+template <int TC, bool TR>
 __global__ void __launch_bounds__(kHeadThreads)
 route_ensure_cluster_kernel(RouteEnsureArgs a) {
+  unsigned long long* const tr = TR ? a.tr : nullptr;
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ EnsureSmem sm;
@@ -454,6 +456,7 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   }
   pdl_wait();
   pdl_trigger();
+  if (crank == 0 && threadIdx.x == 0) trace_max(tr, kTrHeadWait);
   float* to0 = cluster.map_shared_rank(lall, 0);
   float* to1 = cluster.map_shared_rank(lall, pf ? 1 : 0);
   bool waited = false;
@@ -522,6 +525,7 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
   }
   if (!waited) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   cluster.sync();  // every logit is in CTA 0's (and predicted ones in CTA 1's) shared memory
+  if (crank == 0 && threadIdx.x == 0) trace_max(tr, kTrHeadLogits);
   if (pf && crank == 1) {
     // Lookahead into the next layer: predicted top-k, candidates, install.
     for (int t = warp; t < T; t += kHeadWarps) {
@@ -563,7 +567,9 @@ route_ensure_cluster_kernel(RouteEnsureArgs a) {
     }
   }
   __syncthreads();
+  if (threadIdx.x == 0) trace_max(tr, kTrHeadTopk);
   ensure_call(sm, a.tab, ids_s, T * k, E, a.S, a.slot_ids, a.status, a.expert_bytes);
+  if (threadIdx.x == 0) trace_max(tr, kTrHeadDone);
 }
 
 }  // namespace
@@ -580,16 +586,14 @@ static_assert(kHeadSmemAttr + (int)sizeof(EnsureSmem) + kClusterMaxLogits * 4 <=
 cudaError_t route_init_attributes() {
   cudaError_t e = cudaFuncSetAttribute(route_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemMax);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(route_ensure_cluster_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kHeadSmemAttr);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(route_ensure_cluster_kernel<kTokChunk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kHeadSmemAttr);
+  for (auto kern : {route_ensure_cluster_kernel<1, false>, route_ensure_cluster_kernel<kTokChunk, false>,
+                    route_ensure_cluster_kernel<1, true>})
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kHeadSmemAttr);
   if (e == cudaSuccess) {
-    // 16-CTA head clusters where the device holds one (both instantiations).
+    // 16-CTA head clusters where the device holds one (every instantiation).
     int fits = 1;
-    for (auto kern : {route_ensure_cluster_kernel<1>, route_ensure_cluster_kernel<kTokChunk>}) {
+    for (auto kern : {route_ensure_cluster_kernel<1, false>, route_ensure_cluster_kernel<kTokChunk, false>,
+                      route_ensure_cluster_kernel<1, true>}) {
       int n = 0;
       cudaLaunchConfig_t cfg{};
       cfg.gridDim = dim3(16);
@@ -655,8 +659,9 @@ cudaError_t launch_route_ensure(const RouteEnsureArgs& a, cudaStream_t st) {
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.pdl ? 2 : 1;
-    if (T == 1) return cudaLaunchKernelEx(&cfg, route_ensure_cluster_kernel<1>, a);
-    return cudaLaunchKernelEx(&cfg, route_ensure_cluster_kernel<kTokChunk>, a);
+    if (T == 1 && a.tr) return cudaLaunchKernelEx(&cfg, route_ensure_cluster_kernel<1, true>, a);
+    if (T == 1) return cudaLaunchKernelEx(&cfg, route_ensure_cluster_kernel<1, false>, a);
+    return cudaLaunchKernelEx(&cfg, route_ensure_cluster_kernel<kTokChunk, false>, a);
   }
   const int per_cta = kEnsureThreads / 32;
   const int grid = (E + per_cta - 1) / per_cta;

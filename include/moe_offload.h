@@ -439,6 +439,37 @@ moe_status_t moe_offload_host_read_gbs(int device, const void* host_ptr, size_t 
  * they were captured with). */
 moe_status_t moe_offload_debug_wait(moe_offload_t h, long long limit_ns, int stall);
 
+/* ---- Decode trace (observability; no counterpart on the pages) ---------
+ * With the trace on, decode-path launches enqueued afterwards (eager
+ * moe_offload_decode_layer, and decode graphs created afterwards) stamp
+ * %globaltimer (nanoseconds) into a per-layer record of MOE_TRACE_FIELDS
+ * uint64 words: the earliest (fields marked min) or latest time a kernel of that
+ * layer passed a point of the step. Layer records accumulate over calls until
+ * read with reset, so read (and reset) after every step to see one call.
+ * Field order (values of the TraceField enumeration of the kernels):
+ *   0 head CTA 0 past its dependency wait      1 head logits complete
+ *   2 head top-k and weights written           3 head slot table updated
+ *   4 gate/up first CTA past its wait (min)    5 first W2 bytes of an installed expert in (min)
+ *   6 last gate/up CTA of an installed expert  7 last W2-copy CTA done
+ *   8 last gate/up CTA done                    9 down first CTA started (min)
+ *  10 down last CTA past its waits             11 down last CTA done
+ *  12-15 unused. Fields 4, 5 and 9 read ~0 and the others 0 when nothing stamped.
+ * Only one-token calls (T = 1) are traced, through traced variants of the three
+ * decode kernels (the plain ones carry no stamp code; the traced FFN variants
+ * spill a few more registers, so a traced step is not the timed one). */
+#define MOE_TRACE_FIELDS 16
+
+/* on = 1: allocate the layer records (L * MOE_TRACE_FIELDS uint64 on the
+ * device, once per handle), reset them and stamp from now on; on = 0: stop
+ * (the records stay). Host only, no synchronisation beyond the reset.
+ * Errors: MOE_ERR_INVALID, MOE_ERR_OOM, MOE_ERR_CUDA. */
+moe_status_t moe_offload_trace_enable(moe_offload_t h, int on);
+
+/* Copy the layer records into out[L * MOE_TRACE_FIELDS] (host), after
+ * synchronising the device; reset = 1 then sets them back to their unset
+ * values. MOE_ERR_INVALID when the trace was never enabled. */
+moe_status_t moe_offload_trace_read(moe_offload_t h, uint64_t* out, int reset);
+
 /* ---- Decode step as one CUDA graph -------------------------------------
  * A decode step of the whole stack (moe_offload_decode_layer for layers
  * 0..L-1 at batch T, layer l reading x + l*T*H and writing out + l*T*H) is

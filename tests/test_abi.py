@@ -104,6 +104,9 @@ def test_null_handle_calls_are_rejected(lib):
     assert lib.moe_offload_get_config(None, None, None) == C.MOE_ERR_INVALID
     assert lib.moe_offload_read_routing(None, None, None, None, 0, None) == C.MOE_ERR_INVALID
     assert lib.moe_offload_debug_wait(None, 0, 0) == C.MOE_ERR_INVALID
+    assert lib.moe_offload_trace_enable(None, 1) == C.MOE_ERR_INVALID
+    assert lib.moe_offload_trace_read(None, None, 0) == C.MOE_ERR_INVALID
+    assert C.MOE_TRACE_FIELDS >= len(C.TRACE_FIELD_NAMES) and set(C.TRACE_MIN_FIELDS) <= set(C.TRACE_FIELD_NAMES)
     lib.moe_offload_destroy(None)
 
 
