@@ -298,6 +298,59 @@ def cpu_oracle_rate(store, x, seconds):
     return tokens / dt, tokens, oracle.num_threads(), dt
 
 
+def trace_pass(P, cfg, xdev, tokens, skip=16):
+    """Untimed: the decode graph with the trace on (moe_offload_trace_enable), one
+    token at a time from an empty table, records read after each token. Returns, for
+    layer calls with and without installed experts after the first `skip` tokens, the
+    median of each segment of a layer in microseconds."""
+    import numpy as np
+    import torch
+    from expert_cache_router_gb300 import DecodeGraph, _lib as C
+    moe, L, H = P.moe, cfg.num_layers, cfg.hidden
+    f = {n: i for i, n in enumerate(C.TRACE_FIELD_NAMES)}
+    gx = torch.zeros((L, 1, H), dtype=torch.int16, device=xdev.device)
+    go = torch.zeros_like(gx)
+    P.restart()
+    moe.trace_enable(True)
+    g = DecodeGraph(moe, 1, gx, go)
+    rows = {True: [], False: []}
+    try:
+        for t in range(tokens):
+            gx.copy_(xdev[t])
+            g.launch(P.stream)
+            rec = moe.trace_read(reset=True).astype(np.float64) / 1e3   # us
+            if t < skip:
+                continue
+            for l in range(1, L):
+                r, prev = rec[l], rec[l - 1]
+                _, n_miss, n_spill = moe.read_misses(l)
+                seg = {"release_after_previous_down": r[f["head_wait"]] - prev[f["down_done"]],
+                       "head": r[f["head_done"]] - r[f["head_wait"]],
+                       "head_to_gate_up": r[f["gate_first"]] - r[f["head_done"]],
+                       "gate_up": r[f["gate_done"]] - r[f["gate_first"]],
+                       "down_tail_after_gate_up": r[f["down_done"]] - r[f["gate_done"]],
+                       "layer": r[f["down_done"]] - prev[f["down_done"]]}
+                if n_miss - n_spill > 0:
+                    seg["first_host_bytes_after_gate_up_start"] = r[f["host_first"]] - r[f["gate_first"]]
+                    seg["host_stream_end_to_gate_up_end"] = r[f["gate_done"]] - max(r[f["copy_done"]],
+                                                                                    r[f["host_done"]])
+                rows[n_miss - n_spill > 0].append(seg)
+    finally:
+        g.close()
+        moe.trace_enable(False)
+        torch.cuda.synchronize()
+
+    def med(rs):
+        keys = sorted({k for r in rs for k in r})
+        return {k: round(float(np.median([r[k] for r in rs if k in r])), 2) for k in keys}
+    return {"tokens": tokens, "skipped": skip, "layer_calls_with_installs": len(rows[True]),
+            "layer_calls_without": len(rows[False]), "with_installs_us": med(rows[True]),
+            "without_installs_us": med(rows[False]),
+            "how": "globaltimer stamps of the traced one-token kernels (moe_offload_trace_read), medians over "
+                   "layers 1..L-1 of every token after the first `skipped`; untimed: a traced step runs "
+                   "slightly slower than the timed one"}
+
+
 def prefill_pass(args, cfg, moe, store, dev, stream):
     """Prefill of one prompt through every layer (the staging path when a layer's
     distinct experts outnumber its slots), then 64 decode tokens on the slots.
@@ -705,6 +758,9 @@ def run_ours(args, dist):
                                   full=(B == 1), sampler=ClockSampler(dist.local) if B == 1 else None,
                                   e2e=(B == 1 and not args.no_e2e))
 
+    trace = None
+    if not static and dist.rank == 0:
+        trace = trace_pass(P, cfg, xs[1][1], min(K, 64))
     r1 = results[1]
     world = dist.world
     stats = r1["stats"]
@@ -745,6 +801,8 @@ def run_ours(args, dist):
         line["e2e"] = {"value": world * K / r1["e2e_secs"], "unit": "tok/s", "h2d_bytes_per_step": nbytes,
                        "d2h_bytes_per_step": nbytes,
                        "path": "moe_offload_graph_launch_host: pinned host in, graph replay, pinned host out, per step"}
+    if trace is not None:
+        line["trace"] = trace
     if not args.no_prefill and cfg.num_experts > cfg.num_slots and not static:
         line["prefill"] = prefill_pass(args, cfg, moe, store, dev, stream)
     moe.close()
