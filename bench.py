@@ -328,7 +328,8 @@ def trace_pass(P, cfg, xdev, tokens, skip=16):
                        "head": r[f["head_done"]] - r[f["head_wait"]],
                        "head_to_gate_up": r[f["gate_first"]] - r[f["head_done"]],
                        "gate_up": r[f["gate_done"]] - r[f["gate_first"]],
-                       "down_tail_after_gate_up": r[f["down_done"]] - r[f["gate_done"]],
+                       "down_tail_after_gate_up": r[f["down_out"]] - r[f["gate_done"]],
+                       "down_waits_after_gate_up": r[f["down_waits"]] - r[f["gate_done"]],
                        "layer": r[f["down_done"]] - prev[f["down_done"]]}
                 if n_miss - n_spill > 0:
                     seg["first_host_bytes_after_gate_up_start"] = r[f["host_first"]] - r[f["gate_first"]]

@@ -17,7 +17,7 @@ MOE_DEV_BAD_EXPERT_ID, MOE_DEV_BAD_SLOT_ID, MOE_DEV_AUDIT_FAILED, MOE_DEV_BAD_CO
 MOE_TRACE_FIELDS = 16
 # decode trace record fields (moe_offload_trace_read), in order
 TRACE_FIELD_NAMES = ("head_wait", "head_logits", "head_topk", "head_done", "gate_first", "host_first",
-                     "host_done", "copy_done", "gate_done", "down_first", "down_waits", "down_done")
+                     "host_done", "copy_done", "gate_done", "down_first", "down_waits", "down_done", "down_out")
 TRACE_MIN_FIELDS = ("gate_first", "host_first", "down_first")
 
 # Every symbol the header declares, in declaration order.

@@ -136,13 +136,14 @@ enum TraceField {
   kTrHeadTopk,          // head, top-k and weights written
   kTrHeadDone,          // head, slot table updated
   kTrGateFirst,         // gate/up, first CTA past its dependency wait        (min)
-  kTrGateHostFirst,     // gate/up, first W2 bytes of an installed expert in   (min)
+  kTrGateHostFirst,     // gate/up, first W13 chunk of an installed expert used (min)
   kTrGateHostDone,      // gate/up, last CTA of an installed expert done      (max)
   kTrCopyDone,          // gate/up, last W2-copy CTA done                     (max)
   kTrGateDone,          // gate/up, last CTA done                             (max)
   kTrDownFirst,         // down, first CTA started                            (min)
   kTrDownWaits,         // down, last CTA past its waits                      (max)
-  kTrDownDone,          // down, last CTA done                                (max)
+  kTrDownDone,          // down, last CTA done (counter resets included)      (max)
+  kTrDownOut,           // down, latest CTA past writing its output rows      (max)
   kTraceFields = 16
 };
 constexpr unsigned kTraceMinFields =

@@ -242,7 +242,7 @@ __device__ void form_group(const FfnArgs& a, int* sid, int* members, Group* g, b
 
 // Copy-through workers: W2 (and FP8 scales) of every expert installed by this call, host -> slot.
 template <int FMT>
-__device__ void copy_installed_rest(const FfnArgs& a, int worker, int workers, unsigned long long* tr) {
+__device__ void copy_installed_rest(const FfnArgs& a, int worker, int workers) {
   const int n = min(__ldcg(a.counts + kCntInstall), a.S);
   if (n <= 0) return;
   const ExpertSizes z = sizes_of<FMT>(a);
@@ -284,7 +284,6 @@ __device__ void copy_installed_rest(const FfnArgs& a, int worker, int workers, u
 #pragma unroll
     for (int q = 0; q < U; ++q)
       if (d[q]) *d[q] = v[q];
-    if (u0 == t0 && threadIdx.x == 0) trace_min(tr, kTrGateHostFirst);  // first host bytes arrived
   }
 }
 
@@ -305,7 +304,7 @@ ffn_gate_up_kernel(FfnArgs a) {
   const int Tk = a.T * a.k;
   const int cols = Tk + (a.shared ? 1 : 0);
   if ((int)blockIdx.x >= cols) {  // copy-through W2 workers
-    copy_installed_rest<FMT>(a, (blockIdx.x - cols) * gridDim.y + blockIdx.y, (gridDim.x - cols) * gridDim.y, tr);
+    copy_installed_rest<FMT>(a, (blockIdx.x - cols) * gridDim.y + blockIdx.y, (gridDim.x - cols) * gridDim.y);
     signal_done(a.sync, kSyncCopy);
     if (threadIdx.x == 0) {
       trace_max(tr, kTrCopyDone);
@@ -402,6 +401,10 @@ ffn_gate_up_kernel(FfnArgs a) {
             }
           }
         }
+        // first host chunk of an installed expert used: the test reads acc, so the
+        // stamp follows the chunk's arrival (it is skipped only if acc hits that value)
+        if (TR && dst && c0 == lane * CE && threadIdx.x == 0 && acc[0][0] != 1.2345e-7f)
+          trace_min(tr, kTrGateHostFirst);
       }
     }
 #pragma unroll
@@ -429,8 +432,9 @@ ffn_gate_up_kernel(FfnArgs a) {
 // expert) and dot each of the 8 W2 rows with h of every pair routed to that
 // slot; the CTA then sums the k ranks of each token in rank order (and the
 // shared expert last, weight 1). No other CTA touches these rows.
+// (The traced one-token variant is held to two CTAs per SM, the occupancy of the plain one.)
 template <int FMT, int TC, bool TR>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, (TR && TC == 1) ? 2 : 0)
 ffn_down_combine_kernel(FfnArgs a) {
   unsigned long long* const tr = TR ? a.tr : nullptr;
   extern __shared__ float ys[];       // [Tk (+T)][kDownRowsPerCta]
@@ -635,6 +639,7 @@ ffn_down_combine_kernel(FfnArgs a) {
     const __nv_bfloat16 b = __float2bfloat16_rn(acc);
     a.out[(size_t)t * H + r0 + r] = *reinterpret_cast<const uint16_t*>(&b);
   }
+  if (threadIdx.x == 0) trace_max(tr, kTrDownOut);  // thread 0's rows written
   if (a.sync && s_last) {  // every down CTA is past its waits: let the gate/up grid complete, reset
     if (threadIdx.x == 0) {
       if (copy_ctas) wait_at_least(a.sync + kSyncCopy, copy_ctas, a.status, wait_ns);

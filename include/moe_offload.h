@@ -449,11 +449,12 @@ moe_status_t moe_offload_debug_wait(moe_offload_t h, long long limit_ns, int sta
  * Field order (values of the TraceField enumeration of the kernels):
  *   0 head CTA 0 past its dependency wait      1 head logits complete
  *   2 head top-k and weights written           3 head slot table updated
- *   4 gate/up first CTA past its wait (min)    5 first W2 bytes of an installed expert in (min)
+ *   4 gate/up first CTA past its wait (min)    5 first W13 chunk of an installed expert used (min)
  *   6 last gate/up CTA of an installed expert  7 last W2-copy CTA done
  *   8 last gate/up CTA done                    9 down first CTA started (min)
- *  10 down last CTA past its waits             11 down last CTA done
- *  12-15 unused. Fields 4, 5 and 9 read ~0 and the others 0 when nothing stamped.
+ *  10 down last CTA past its waits             11 down last CTA done (counter resets included)
+ *  12 down, latest CTA past writing its rows   13-15 unused.
+ * Fields 4, 5 and 9 read ~0 and the others 0 when nothing stamped.
  * Only one-token calls (T = 1) are traced, through traced variants of the three
  * decode kernels (the plain ones carry no stamp code; the traced FFN variants
  * spill a few more registers, so a traced step is not the timed one). */

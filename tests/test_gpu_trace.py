@@ -67,6 +67,7 @@ def test_decode_trace_is_ordered_and_changes_no_output(dev):
                 assert r[f["gate_first"]] != unset_min and r[f["down_first"]] != unset_min
                 assert all(a <= b for a, b in zip(order, order[1:])), (t, l, order)
                 assert r[f["down_first"]] <= r[f["down_done"]] and r[f["down_waits"]] <= r[f["down_done"]]
+                assert r[f["down_waits"]] <= r[f["down_out"]] <= r[f["down_done"]]
                 if l + 1 < st.cfg.num_layers:  # the next head passes its wait after this down completes
                     assert rec[l + 1][f["head_wait"]] >= r[f["down_done"]]
                 if inst[l] > 0:
