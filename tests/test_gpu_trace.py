@@ -73,8 +73,9 @@ def test_decode_trace_is_ordered_and_changes_no_output(dev):
                 if inst[l] > 0:
                     seen_install = True
                     assert r[f["host_first"]] != unset_min and r[f["gate_first"]] <= r[f["host_first"]]
-                    assert r[f["host_first"]] <= r[f["copy_done"]] <= r[f["gate_done"]]
-                    assert r[f["host_done"]] <= r[f["gate_done"]]
+                    # the W2 copy may finish before the installed expert's first W13 chunk is used
+                    assert r[f["host_first"]] <= r[f["host_done"]] <= r[f["gate_done"]]
+                    assert r[f["copy_done"]] <= r[f["gate_done"]]
                 else:
                     assert r[f["host_first"]] == unset_min
         assert seen_install
