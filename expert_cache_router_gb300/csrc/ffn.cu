@@ -432,12 +432,12 @@ ffn_gate_up_kernel(FfnArgs a) {
 // expert) and dot each of the 8 W2 rows with h of every pair routed to that
 // slot; the CTA then sums the k ranks of each token in rank order (and the
 // shared expert last, weight 1). No other CTA touches these rows.
-// (The traced one-token variant is held to two CTAs per SM, the occupancy of the plain one.)
+// (The one-token variants are held to two CTAs per SM, 128 registers.)
 template <int FMT, int TC, bool TR>
-__global__ void __launch_bounds__(kThreads, (TR && TC == 1) ? 2 : 0)
+__global__ void __launch_bounds__(kThreads, TC == 1 ? 2 : 0)
 ffn_down_combine_kernel(FfnArgs a) {
   unsigned long long* const tr = TR ? a.tr : nullptr;
-  extern __shared__ float ys[];       // [Tk (+T)][kDownRowsPerCta]
+  extern __shared__ float ys[];       // [parts][Tk (+T)][kDownRowsPerCta]
   __shared__ int sid[kMaxPairs];
   __shared__ int nxt[kMaxPairs];      // next pair routed to the same slot, -1 at the end
   __shared__ int glead[kMaxPairs];    // first pair of each distinct slot, in pair order
@@ -516,6 +516,13 @@ ffn_down_combine_kernel(FfnArgs a) {
   const int r0 = blockIdx.x * kDownRowsPerCta;
   const int ib = I >> 7;
   const int ngroups = s_groups + (a.shared ? 1 : 0);
+  // One token with fewer expert groups than warps (a small top-k, e.g. 2): each
+  // group's I range is split over `parts` warps, whole loop steps each, and the
+  // partial sums are added in part order in the combine. With one part this is
+  // the plain per-group loop.
+  const int parts = (TC == 1 && a.T == 1 && ngroups > 0 && ngroups < kWarps) ? kWarps / ngroups : 1;
+  const int items = ngroups * parts;
+  const int npairs = Tk + (a.shared ? a.T : 0);
   // Early down: the CTA counts itself done once every warp is past its last
   // wait, so that round trip overlaps the compute; the CTA that counts last
   // resets the counters at its end.
@@ -525,8 +532,10 @@ ffn_down_combine_kernel(FfnArgs a) {
       trace_max(tr, kTrDownWaits);
     }
   };
-  if (warp >= ngroups) waits_done();
-  for (int d = warp; d < ngroups; d += kWarps) {
+  if (warp >= items) waits_done();
+  for (int item = warp; item < items; item += kWarps) {
+    const int d = parts == 1 ? item : item % ngroups, part = parts == 1 ? 0 : item / ngroups;
+    float* ysp = ys + (size_t)part * npairs * kDownRowsPerCta;  // this part's partial sums
     const uint8_t* w2 = nullptr;
     const float* s2 = nullptr;
     int p0;
@@ -559,7 +568,7 @@ ffn_down_combine_kernel(FfnArgs a) {
           filled)
         wait_at_least(a.sync + kSyncCopy, copy_ctas, a.status, wait_ns);
       __syncwarp();
-      if (d + kWarps >= ngroups) waits_done();
+      if (item + kWarps >= items) waits_done();
     }
     const bool coh = a.sync && filled;
     for (int p = p0; p >= 0;) {
@@ -575,7 +584,7 @@ ffn_down_combine_kernel(FfnArgs a) {
       }
       if (!w2) {
         for (int t = 0; t < nt; ++t)
-          if (lane < kDownRowsPerCta) ys[mem[t] * kDownRowsPerCta + lane] = 0.0f;
+          if (lane < kDownRowsPerCta) ysp[mem[t] * kDownRowsPerCta + lane] = 0.0f;
         continue;
       }
       float acc[kDownRowsPerCta][TC];
@@ -584,7 +593,10 @@ ffn_down_combine_kernel(FfnArgs a) {
 #pragma unroll
         for (int t = 0; t < TC; ++t) acc[r][t] = 0.0f;
       constexpr int UNR = FMT == 1 ? 1 : (TC <= 2 ? 3 : 1);
-      for (int c0 = lane * CE; c0 < I; c0 += 32 * CE * UNR) {
+      constexpr int kStep = 32 * CE * UNR;  // columns of one loop step
+      const int span = (I + parts * kStep - 1) / (parts * kStep) * kStep;
+      const int i_lo = part * span, i_hi = min(I, i_lo + span);
+      for (int c0 = i_lo + lane * CE; c0 < i_hi; c0 += kStep) {
         uint4 wv[UNR][kDownRowsPerCta];
         float sc[UNR][kDownRowsPerCta];
 #pragma unroll
@@ -623,7 +635,7 @@ ffn_down_combine_kernel(FfnArgs a) {
 #pragma unroll
         for (int r = 0; r < kDownRowsPerCta; ++r) {
           const float yv = warp_sum(acc[r][t]);
-          if (lane == 0 && t < nt) ys[mem[t] * kDownRowsPerCta + r] = yv;
+          if (lane == 0 && t < nt) ysp[mem[t] * kDownRowsPerCta + r] = yv;
         }
       }
     }
@@ -632,10 +644,14 @@ ffn_down_combine_kernel(FfnArgs a) {
   const int rows = min(kDownRowsPerCta, H - r0);
   for (int idx = threadIdx.x; idx < a.T * rows; idx += kThreads) {
     const int t = idx / rows, r = idx - t * rows;
+    auto y_of = [&](int pair) {  // the pair's y row, its parts added in order
+      float y = ys[pair * kDownRowsPerCta + r];
+      for (int q = 1; q < parts; ++q) y = __fadd_rn(y, ys[((size_t)q * npairs + pair) * kDownRowsPerCta + r]);
+      return y;
+    };
     float acc = 0.0f;
-    for (int j = 0; j < k; ++j)
-      acc = __fadd_rn(acc, __fmul_rn(s_w[t * k + j], ys[(t * k + j) * kDownRowsPerCta + r]));
-    if (a.shared) acc = __fadd_rn(acc, ys[(Tk + t) * kDownRowsPerCta + r]);
+    for (int j = 0; j < k; ++j) acc = __fadd_rn(acc, __fmul_rn(s_w[t * k + j], y_of(t * k + j)));
+    if (a.shared) acc = __fadd_rn(acc, y_of(Tk + t));
     const __nv_bfloat16 b = __float2bfloat16_rn(acc);
     a.out[(size_t)t * H + r0 + r] = *reinterpret_cast<const uint16_t*>(&b);
   }
@@ -667,7 +683,8 @@ cudaError_t launch_tc(const FfnArgs& a, int phase, cudaStream_t st) {
     if (TC == 1 && a.tr) return launch_k(ffn_gate_up_kernel<FMT, 1, true>, g1, dim3(kThreads), 0, st, a.pdl != 0, a);
     return launch_k(ffn_gate_up_kernel<FMT, TC, false>, g1, dim3(kThreads), 0, st, a.pdl != 0, a);
   }
-  const size_t smem = (size_t)(Tk + (a.shared ? a.T : 0)) * kDownRowsPerCta * sizeof(float);
+  // one token: room for the partial sums of up to kWarps parts per group
+  const size_t smem = (size_t)(Tk + (a.shared ? a.T : 0)) * kDownRowsPerCta * sizeof(float) * (a.T == 1 ? kWarps : 1);
   const dim3 g2((a.H + kDownRowsPerCta - 1) / kDownRowsPerCta);
   if (TC == 1 && a.tr)
     return launch_k(ffn_down_combine_kernel<FMT, 1, true>, g2, dim3(kThreads), smem, st, a.pdl != 0, a);
