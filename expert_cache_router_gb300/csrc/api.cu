@@ -50,8 +50,6 @@ struct moe_offload {
   int pdl = 1;  // programmatic dependent launch in the decode chain (env MOE_OFFLOAD_PDL=0 turns it off)
   int audit_each = 0;  // env MOE_OFFLOAD_AUDIT=1: audit a layer's table after every update of it
   int early_down = 1;  // env MOE_OFFLOAD_EARLY_DOWN=0: the down launch waits for the whole gate/up grid
-  int pf_device_join = 1;  // env MOE_OFFLOAD_PF_DEVICE_JOIN=0: the decode FFN waits (stream event) for the
-                           // whole prefetch copy into its layer instead of joining it on the device
   unsigned long long* trace = nullptr;  // [L, kTraceFields] decode trace records (moe_offload_trace_enable)
   int trace_on = 0;
   uint32_t* ffn_sync = nullptr;  // [kFfnSyncWords] counters of the early-down hand-off
@@ -244,7 +242,6 @@ moe_status_t pf_fork(moe_offload* h, int layer, cudaStream_t st) {
   a.f13 = h->f13;
   a.f2 = h->f2;
   a.status = h->status;
-  a.done_counts = h->tab[layer].counts;  // the device-side join of the decode FFN reads it
   CK(h, launch_miss_copy(a, h->pf_grid, h->pf_stream));
   CK(h, cudaEventRecord(h->pf_done[layer], h->pf_stream));
   h->pf_pending[layer] = capturing(st) ? 2 : 1;
@@ -388,22 +385,11 @@ int launches_per_layer(const moe_offload* h, int layer) {
   return 3 + (h->audit_each ? 1 + (lookahead_on(h, layer) ? 1 : 0) : 0);
 }
 
-// The decode FFN of a layer that receives lookahead prefetches joins the prefetch
-// copy on the device (only CTAs touching a slot of the install wait for it), so
-// the gate/up launch follows the head without a stream dependency in between;
-// returns whether it does (else the caller joins on the stream first).
-bool set_pf_device_join(const moe_offload* h, int layer, FfnArgs* a) {
-  if (!h->pf_device_join || h->cfg.prefetch_n <= 0 || layer < 1) return false;
-  a->pf_counts = h->tab[layer].counts;
-  a->pf_slot = h->tab[layer].pf_slot;
-  return true;
-}
-
 moe_status_t do_decode_ffn(moe_offload* h, int layer, const void* x, int T, void* out, cudaStream_t st,
                            cudaEvent_t after_gate_up = nullptr) {
-  moe_status_t js;
+  moe_status_t js = pf_join(h, layer, st);
+  if (js != MOE_OK) return js;
   FfnArgs a = ffn_args(h, layer, x, h->slot_buf, h->w_buf, T, out);
-  if (!set_pf_device_join(h, layer, &a) && (js = pf_join(h, layer, st)) != MOE_OK) return js;
   a.copy_through = 1;
   a.pdl = h->pdl;
   a.sync = early_down_sync(h, a.pdl);
@@ -414,9 +400,6 @@ moe_status_t do_decode_ffn(moe_offload* h, int layer, const void* x, int T, void
   if (lookahead_on(h, layer) && (js = pf_fork(h, layer + 1, st)) != MOE_OK) return js;
   if (after_gate_up) CK(h, cudaEventRecord(after_gate_up, st));
   CK(h, launch_grouped_ffn_phase(a, 1, st));
-  // A copy joined on the device still rejoins the stream, after the down launch, so
-  // that an eager step leaves no copy pending (the decode graph does it at its end).
-  if (a.pf_counts && (js = pf_join(h, layer, st)) != MOE_OK) return js;
   return MOE_OK;
 }
 
@@ -585,7 +568,6 @@ moe_status_t moe_offload_create(const moe_offload_config_t* cfg, int device, voi
   if (const char* v = getenv("MOE_OFFLOAD_PDL")) h->pdl = atoi(v) != 0;
   if (const char* v = getenv("MOE_OFFLOAD_AUDIT")) h->audit_each = atoi(v) != 0;
   if (const char* v = getenv("MOE_OFFLOAD_EARLY_DOWN")) h->early_down = atoi(v) != 0;
-  if (const char* v = getenv("MOE_OFFLOAD_PF_DEVICE_JOIN")) h->pf_device_join = atoi(v) != 0;
   if (const char* v = getenv("MOE_OFFLOAD_PROFILE")) h->profile = atoi(v) != 0;
   h->prof_sum.assign(c.num_layers, std::array<double, 4>{0.0, 0.0, 0.0, 0.0});
   if (const char* v = getenv("MOE_OFFLOAD_FAIL_ALLOC")) h->fail_alloc_at = atoi(v);
@@ -1399,8 +1381,8 @@ moe_status_t capture_step(moe_offload* h, moe_offload_graph* g, cudaStream_t cs)
     CK(h, mark(4 * l + 0));
     if ((st = do_decode_head(h, l, x, T, cs, !g->timing)) != MOE_OK) return st;
     CK(h, mark(4 * l + 1));
+    if ((st = pf_join(h, l, cs)) != MOE_OK) return st;
     FfnArgs a = ffn_args(h, l, x, h->slot_buf, h->w_buf, T, out);
-    if (!set_pf_device_join(h, l, &a) && (st = pf_join(h, l, cs)) != MOE_OK) return st;
     a.copy_through = 1;
     a.pdl = g->timing ? 0 : h->pdl;  // event nodes sit between the launches of a timing graph
     a.sync = early_down_sync(h, a.pdl);
@@ -1410,9 +1392,6 @@ moe_status_t capture_step(moe_offload* h, moe_offload_graph* g, cudaStream_t cs)
     CK(h, launch_grouped_ffn_phase(a, 1, cs));
     CK(h, mark(4 * l + 3));
   }
-  // Copies joined on the device still have to rejoin the captured stream.
-  for (int l = 0; l < L; ++l)
-    if ((st = pf_join(h, l, cs)) != MOE_OK) return st;
   return MOE_OK;
 }
 

@@ -22,12 +22,8 @@ enum StatIdx { kStatCalls = 0, kStatHits, kStatMisses, kStatSpills, kStatBytesCo
 // Indices into LayerTables::counts (results of the last slot_ensure, and of the
 // last prefetch install into this layer).
 // kCntFrozen (written by the host only): 1 while the layer holds a static placement.
-// kCntPfIssued counts the lookahead installs into the layer (one per install call),
-// kCntPfDone the prefetch copies into it that have completed (one per copy launch,
-// counted by its last CTA, kCntPfCtas being that launch's CTA count): a kernel that
-// touches a slot of the last install waits until done reaches issued.
 enum CountIdx { kCntMiss = 0, kCntSpill, kCntInstall, kCntDistinct, kCntPrefetch, kCntCandidates, kCntFrozen,
-                kCntPfIssued, kCntPfDone, kCntPfCtas, kNumCounts };
+                kNumCounts };
 
 // Device-resident LRU slot table and miss list of one layer.
 struct LayerTables {

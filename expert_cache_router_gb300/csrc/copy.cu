@@ -20,11 +20,11 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kUnroll = 8;
 
-__device__ __forceinline__ void copy_installs(const LayerWeights& lw, const int32_t* __restrict__ counts,
-                                              int count_idx, const int32_t* __restrict__ miss_expert,
-                                              const int32_t* __restrict__ miss_slot, int E, int S,
-                                              unsigned long long u13, unsigned long long u2,
-                                              unsigned long long f13, unsigned long long f2, uint32_t* status) {
+__global__ void __launch_bounds__(kThreads)
+miss_copy_kernel(LayerWeights lw, const int32_t* __restrict__ counts, int count_idx,
+                 const int32_t* __restrict__ miss_expert, const int32_t* __restrict__ miss_slot,
+                 int E, int S, unsigned long long u13, unsigned long long u2, unsigned long long f13,
+                 unsigned long long f2, uint32_t* status) {
   const int n = counts[count_idx];
   if (n <= 0) return;
   if (n > S) {
@@ -88,28 +88,6 @@ __device__ __forceinline__ void copy_installs(const LayerWeights& lw, const int3
   if (bad) atomicOr(status, kDevBadCount);
 }
 
-// done_counts (a prefetch copy; nullptr otherwise): the layer's counts, whose
-// kCntPfDone the last CTA of the launch advances once every CTA's copies are
-// written (the last-block pattern: each CTA fences, then counts itself).
-__global__ void __launch_bounds__(kThreads)
-miss_copy_kernel(LayerWeights lw, const int32_t* __restrict__ counts, int count_idx,
-                 const int32_t* __restrict__ miss_expert, const int32_t* __restrict__ miss_slot,
-                 int E, int S, unsigned long long u13, unsigned long long u2, unsigned long long f13,
-                 unsigned long long f2, uint32_t* status, int32_t* done_counts) {
-  copy_installs(lw, counts, count_idx, miss_expert, miss_slot, E, S, u13, u2, f13, f2, status);
-  if (done_counts) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      if (atomicAdd(done_counts + kCntPfCtas, 1) == (int)gridDim.x - 1) {
-        done_counts[kCntPfCtas] = 0;
-        __threadfence();
-        atomicAdd(done_counts + kCntPfDone, 1);
-      }
-    }
-  }
-}
-
 // One read of every 16-byte unit (or 4-byte unit, for arrays that are not
 // 16-byte aligned and sized) of a mapped host array. The OR of what was read
 // goes to *sink so the loads are kept.
@@ -152,7 +130,7 @@ cudaError_t launch_host_touch(const void* p, unsigned long long bytes, unsigned*
 cudaError_t launch_miss_copy(const CopyArgs& a, int grid, cudaStream_t st) {
   if (a.count_idx < 0 || a.count_idx >= kNumCounts) return cudaErrorInvalidValue;
   miss_copy_kernel<<<grid, kThreads, 0, st>>>(a.lw, a.counts, a.count_idx, a.miss_expert, a.miss_slot, a.E,
-                                              a.S, a.u13, a.u2, a.f13, a.f2, a.status, a.done_counts);
+                                              a.S, a.u13, a.u2, a.f13, a.f2, a.status);
   return cudaGetLastError();
 }
 

@@ -452,7 +452,6 @@ static __device__ void install_block(EnsureSmem& sm, LayerTables tab, const int*
   if (tid == 0) {
     tab.counts[kCntPrefetch] = ninst;
     tab.counts[kCntCandidates] = ncand;
-    atomicAdd(&tab.counts[kCntPfIssued], 1);  // a prefetch copy of this install follows
     atomicAdd(&tab.stats[kStatPrefetchInstalls], (unsigned long long)ninst);
     atomicAdd(&tab.stats[kStatPrefetchBytes], (unsigned long long)ninst * expert_bytes);
   }

@@ -102,27 +102,6 @@ __device__ __forceinline__ uint4 ld_l2(const void* p) {
   return v;
 }
 
-// Device-side join with the prefetch copy into this layer (a.pf_counts set): is
-// slot s one the last lookahead install wrote (its bytes may still be arriving)?
-__device__ __forceinline__ bool slot_prefetched(const FfnArgs& a, int s) {
-  const int n = min(__ldcg(a.pf_counts + kCntPrefetch), a.S);
-  bool hit = false;
-  for (int i = 0; i < n; ++i) hit |= __ldcg(a.pf_slot + i) == s;
-  return hit;
-}
-
-// The whole CTA: when `need` (the same in every thread), thread 0 waits (bounded)
-// until every prefetch copy issued into this layer has completed.
-__device__ __forceinline__ void join_prefetch(const FfnArgs& a, bool need) {
-  if (!need) return;
-  if (threadIdx.x == 0) {
-    const uint32_t target = (uint32_t)__ldcg(a.pf_counts + kCntPfIssued);
-    wait_at_least(reinterpret_cast<const uint32_t*>(a.pf_counts + kCntPfDone), target, a.status,
-                  a.wait_ns ? a.wait_ns : kDefaultWaitNs);
-  }
-  __syncthreads();
-}
-
 // Early down: this CTA's part of a gate/up column (or of the W2 copy) is written.
 __device__ __forceinline__ void signal_done(uint32_t* sync, int word) {
   if (!sync) return;
@@ -325,17 +304,6 @@ ffn_gate_up_kernel(FfnArgs a) {
   const int Tk = a.T * a.k;
   const int cols = Tk + (a.shared ? 1 : 0);
   if ((int)blockIdx.x >= cols) {  // copy-through W2 workers
-    if (a.pf_counts) {  // an install into a slot the prefetch copy may still be writing
-      __shared__ int s_need;
-      if (threadIdx.x == 0) {
-        const int ni = min(__ldcg(a.counts + kCntInstall), a.S);
-        bool need = false;
-        for (int i = 0; i < ni; ++i) need |= slot_prefetched(a, __ldcg(a.miss_slot + i));
-        s_need = need;
-      }
-      __syncthreads();
-      join_prefetch(a, s_need != 0);
-    }
     copy_installed_rest<FMT>(a, (blockIdx.x - cols) * gridDim.y + blockIdx.y, (gridDim.x - cols) * gridDim.y);
     signal_done(a.sync, kSyncCopy);
     if (threadIdx.x == 0) {
@@ -362,15 +330,6 @@ ffn_gate_up_kernel(FfnArgs a) {
     __syncthreads();
   }
   if (!g.leader) return;
-  if (a.pf_counts && (int)blockIdx.x < Tk && g.valid) {  // the slot the prefetch copy may be writing
-    __shared__ int s_need;
-    if (threadIdx.x == 0) {
-      const int s = sid[blockIdx.x];
-      s_need = s >= 0 && s < a.S && slot_prefetched(a, s);
-    }
-    __syncthreads();
-    join_prefetch(a, s_need != 0);
-  }
   const int col_word = blockIdx.x * kSyncLine;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int i0 = blockIdx.y * kGateRowsPerCta + warp * kGateRowsPerWarp;
@@ -611,8 +570,7 @@ ffn_down_combine_kernel(FfnArgs a) {
       __syncwarp();
       if (item + kWarps >= items) waits_done();
     }
-    // slots filled during the call (copy CTAs, or the prefetch copy) are read through L2
-    const bool coh = (a.sync && filled) || (a.pf_counts && w2 && d < s_groups && slot_prefetched(a, sid[p0]));
+    const bool coh = a.sync && filled;
     for (int p = p0; p >= 0;) {
       int mem[TC];
       int nt = 0;

@@ -102,7 +102,6 @@ struct CopyArgs {
   uint32_t* status;
   int count_idx;               // counts[count_idx] experts of the lists are copied (kCntInstall,
                                // or kCntPrefetch with the prefetch lists)
-  int32_t* done_counts;        // prefetch copy: the layer's counts (kCntPfDone advanced at the end), or nullptr
 };
 cudaError_t launch_miss_copy(const CopyArgs& a, int grid, cudaStream_t st);
 // Reads every byte of a mapped host array once from the GPU (p 4-byte aligned, bytes a multiple of 4).
@@ -129,13 +128,6 @@ struct FfnArgs {
   uint32_t* sync;           // early down: [kFfnSyncWords] zeroed counters, or nullptr (down waits for
                             // the whole gate/up grid)
   unsigned long long* tr;    // decode trace of this layer ([kTraceFields]) or nullptr
-  // Device-side join with the lookahead's prefetch copy into this layer (nullptr: the host
-  // joined it before the launch): the layer's counts and its last prefetch install list.
-  // A gate/up CTA whose slot is in the list, or a W2-copy CTA installing into one, waits
-  // (bounded) until counts[kCntPfDone] reaches counts[kCntPfIssued]; the down launch reads
-  // such slots through L2.
-  const int32_t* pf_counts;
-  const int32_t* pf_slot;
   unsigned long long wait_ns;  // bound of one early-down wait (0: kDefaultWaitNs)
   int stall;                // debug: the first group's wait of every down warp targets one CTA more
                             // than its column has, so it runs out (tests of the bounded wait)
