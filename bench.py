@@ -58,6 +58,7 @@ def parse():
     p.add_argument("--no-b8", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-trace", action="store_true", help="skip the untimed traced passes")
     p.add_argument("--no-sub", action="store_true",
                    help="skip the Mixtral-8x7B-shape and FP8-lookahead sub-runs of the default workload")
     p.add_argument("--prefill-tokens", type=int, default=2048)
@@ -326,6 +327,9 @@ def trace_pass(P, cfg, xdev, tokens, skip=16):
                 _, n_miss, n_spill = moe.read_misses(l)
                 seg = {"release_after_previous_down": r[f["head_wait"]] - prev[f["down_done"]],
                        "head": r[f["head_done"]] - r[f["head_wait"]],
+                       "head_logits": r[f["head_logits"]] - r[f["head_wait"]],
+                       "head_topk": r[f["head_topk"]] - r[f["head_logits"]],
+                       "head_table": r[f["head_done"]] - r[f["head_topk"]],
                        "head_to_gate_up": r[f["gate_first"]] - r[f["head_done"]],
                        "gate_up": r[f["gate_done"]] - r[f["gate_first"]],
                        "down_tail_after_gate_up": r[f["down_out"]] - r[f["gate_done"]],
@@ -665,9 +669,12 @@ def sub_workload(args, base, variants, K, W, dev, stream, dist, link, hbm_peak, 
             store.cfg = cfg
             moe = store.handle(torch, dev, router, device=dist.local)
             try:
-                r = decode_batch(Passes(moe, dist, stream), cfg, 1, xw, xt, xt_host, K, W, SUB_REPEATS, stream)
+                P = Passes(moe, dist, stream)
+                r = decode_batch(P, cfg, 1, xw, xt, xt_host, K, W, SUB_REPEATS, stream)
                 res[label] = dict(workload=cfg.name, slots=cfg.num_slots, prefetch_n=cfg.prefetch_n,
                                   warmup=W, **summarize(cfg, store, r, K, dist.world, link, hbm_peak))
+                if dist.rank == 0 and not args.no_trace:
+                    res[label]["trace"] = trace_pass(P, cfg, xt, min(K, 64))
             finally:
                 moe.close()
         if cpu_seconds > 0 and dist.rank == 0:
@@ -760,7 +767,7 @@ def run_ours(args, dist):
                                   e2e=(B == 1 and not args.no_e2e))
 
     trace = None
-    if not static and dist.rank == 0:
+    if not static and dist.rank == 0 and not args.no_trace:
         trace = trace_pass(P, cfg, xs[1][1], min(K, 64))
     r1 = results[1]
     world = dist.world
