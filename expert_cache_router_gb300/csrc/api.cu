@@ -49,7 +49,7 @@ struct moe_offload {
   int copy_grid = 0;
   int pdl = 1;  // programmatic dependent launch in the decode chain (env MOE_OFFLOAD_PDL=0 turns it off)
   int audit_each = 0;  // env MOE_OFFLOAD_AUDIT=1: audit a layer's table after every update of it
-  int early_down = 1;  // env MOE_OFFLOAD_EARLY_DOWN=0: the down launch waits for the whole gate/up grid
+  int early_down = 1;  // env MOE_OFFLOAD_EARLY_DOWN=0: the down launch (decode and prefill) waits for the whole gate/up grid
   unsigned long long* trace = nullptr;  // [L, kTraceFields] decode trace records (moe_offload_trace_enable)
   int trace_on = 0;
   uint32_t* ffn_sync = nullptr;  // [kFfnSyncWords] counters of the early-down hand-off
@@ -840,6 +840,7 @@ moe_status_t moe_offload_decode_layer(moe_offload_t h, int layer, const void* x,
   pl.route_done = h->route_done + layer;
   pl.status = h->status;
   pl.frozen = h->frozen[layer];
+  pl.early_down = h->early_down;
   pl.layer = layer;
   pl.next_host_w13 = nullptr;
   pl.next_host_w2 = nullptr;

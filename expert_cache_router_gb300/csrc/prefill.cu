@@ -374,6 +374,8 @@ cudaError_t prefill_reserve(PrefillState* ps, int T, int k, int E, size_t* dev_b
   if ((e = grow(&ps->hb, pairs * ps->I, dev_bytes)) != cudaSuccess) return e;
   if ((e = grow(&ps->xp, pairs * ps->H, dev_bytes)) != cudaSuccess) return e;
   if ((e = grow(&ps->yb, pairs * ps->H, dev_bytes)) != cudaSuccess) return e;
+  // one counter per 128-row tensor-core tile (tiles <= ceil(pairs / 128) + groups)
+  if ((e = grow(&ps->tile_done, (pairs + 127) / 128 + kMaxGroups + 2, dev_bytes)) != cudaSuccess) return e;
   ps->cap_T = T;
   ps->cap_pairs = (int)pairs;
   return cudaSuccess;
@@ -533,6 +535,7 @@ cudaError_t prefill_layer(PrefillState* ps, const PrefillLayer& pl, const uint16
     ta.x = x; ta.perm = ps->perm; ta.counts = ps->meta + kMetaCounts; ta.offsets = ps->meta + kMetaOffsets;
     ta.tiles = ps->meta + kMetaTiles; ta.Tk = P; ta.k = pl.k; ta.Tr = Tk; ta.G = G; ta.H = pl.H; ta.I = pl.I;
     ta.w13 = base13; ta.w2 = base2; ta.xp = ps->xp; ta.hp = ps->hb; ta.y = ps->yb; ta.status = pl.status;
+    ta.tile_done = pl.early_down ? ps->tile_done : nullptr;
     if ((e = launch_tc_prefill(ta, st)) != cudaSuccess) { *why = "tensor-core grouped GEMM"; return e; }
   } else {
     // shapes the 128x256 tensor-core tiling does not cover: CUDA-core tiles
@@ -573,7 +576,7 @@ void prefill_forget(PrefillState* ps) {
 void prefill_destroy(PrefillState* ps) {
   if (ps->stage_stream) cudaStreamSynchronize(ps->stage_stream);
   cudaFree(ps->ids); cudaFree(ps->w); cudaFree(ps->gidx); cudaFree(ps->perm); cudaFree(ps->logits);
-  cudaFree(ps->hb); cudaFree(ps->xp); cudaFree(ps->yb); cudaFree(ps->meta);
+  cudaFree(ps->hb); cudaFree(ps->xp); cudaFree(ps->yb); cudaFree(ps->meta); cudaFree(ps->tile_done);
   for (int b = 0; b < 2; ++b) {
     cudaFree(ps->stage_w13[b]);
     cudaFree(ps->stage_w2[b]);

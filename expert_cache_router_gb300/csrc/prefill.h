@@ -23,6 +23,7 @@ struct PrefillState {
   uint16_t* hb = nullptr;     // [T*k, I] bf16 SiLU(g)*u, in group order
   uint16_t* xp = nullptr;     // [T*k, H] bf16 x rows in group order (tensor-core path)
   float* yb = nullptr;        // [T*k, H] fp32 expert outputs, by pair
+  uint32_t* tile_done = nullptr;  // tensor-core path: per-tile gate/up completion counts (early down)
   // Two whole-layer staging buffers: while one serves a layer's GEMMs, the next
   // layer is staged into the other (speculatively: used if that layer stages too).
   uint16_t* stage_w13[2] = {nullptr, nullptr};  // [E,2I,H]
@@ -67,6 +68,7 @@ struct PrefillLayer {
   unsigned* route_done;
   uint32_t* status;
   int frozen;  // the layer holds a static placement: always stage (its table takes no installs)
+  int early_down;  // tensor-core GEMMs: the down launch starts under gate/up (per-tile counts)
 };
 
 cudaError_t prefill_init_attributes();

@@ -19,6 +19,15 @@
 // weight bytes they stream, so the ring is made of small stages (K = 32,
 // 64-byte swizzle) to keep more bytes in flight per SM.
 //
+// Early down: the down launch follows the gate/up launch under programmatic
+// dependent launch. Each gate/up CTA triggers it at its start and, once its h
+// rows are written, counts itself into its tile's counter; a down CTA issues the
+// weight (W2) loads of its first stages at once and the h-tile loads only when
+// its tile's count is complete (a bounded wait), so down CTAs take the SMs that
+// the gate/up launch's last, partial wave leaves idle. The down grid starts only
+// after every gate/up CTA has started, so a waiting down CTA never keeps a
+// producer off the GPU.
+//
 // Warp roles (4 warps): warp 0 allocates TMEM and, one lane, issues the TMA
 // loads of a shared-memory ring (8 stages for NB = 1, 5 stages of NB weight
 // tiles for NB = 2, K = 32 each); warp 1, one lane, issues tcgen05.mma (M=128, N=256, K=16,
@@ -164,7 +173,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   uint64_t* done = empty + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   __shared__ int s_fail;
+  __shared__ int s_stale;  // early down: the tile's h rows did not arrive in time (no output written)
 
+  if (MODE == 1) pdl_trigger();  // the down launch may start once every gate/up CTA has started
   // blockIdx.x: column block pair, blockIdx.y: row tile. The CTAs of one tile are adjacent in
   // launch order, so they run together and its x (or h) tile is read from DRAM once and then
   // from L2; so are the tiles of one bucket, which share its weights.
@@ -175,6 +186,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 
   if (threadIdx.x == 0) {
     s_fail = 0;
+    s_stale = 0;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -196,7 +208,35 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 
   int issued = 0;  // stages the producer loaded (for the drain on failure)
   if (warp == 0 && lane == 0) {
-    // TMA producer
+    // TMA producer. Stage kb: the A tile (x or h rows) and NB weight tiles.
+    const CUtensorMap* tmb = &tm_b;
+    auto load_b = [&](int kb, uint8_t* a_dst, uint64_t* bar) {
+#pragma unroll
+      for (int ac = 0; ac < NB; ++ac) {
+        uint8_t* b_dst = a_dst + A_BYTES + ac * B_BYTES;
+        const int j = blockIdx.x * NB + ac;  // column block of accumulator ac
+        if (MODE == 1) {
+          const int gate_row = g * 2 * p.I + j * (BN / 2);
+          tma_load_2d(tmb, bar, b_dst, kb * BK, gate_row);
+          tma_load_2d(tmb, bar, b_dst + B_BYTES / 2, kb * BK, gate_row + p.I);
+        } else {
+          tma_load_2d(tmb, bar, b_dst, kb * BK, g * p.H + j * BN);
+        }
+      }
+    };
+    // Early down: the weight tiles of the first stages do not depend on the gate/up
+    // launch and go out at once; the h tiles follow once the tile's count is complete.
+    const int pre = (MODE == 2 && p.tile_done) ? min(nk, STAGES) : 0;
+    for (int kb = 0; kb < pre; ++kb) {
+      mbar_expect_tx(&full[kb], STAGE_BYTES);
+      load_b(kb, smem + kb * STAGE_BYTES, &full[kb]);
+    }
+    if (pre) {
+      // On a timeout (status bit set) every stage is still loaded and consumed, so no
+      // copy is left in flight, and the epilogue writes nothing.
+      if (!wait_at_least(p.tile_done + blockIdx.y, p.tile_need, p.status, kDefaultWaitNs)) s_stale = 1;
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // h rows were written by generic stores
+    }
     for (int kb = 0; kb < nk; ++kb) {
       const int s = kb % STAGES;
       if (kb >= STAGES && !mbar_wait(&empty[s], ((kb / STAGES) - 1) & 1)) {
@@ -205,20 +245,11 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         break;
       }
       uint8_t* a_dst = smem + s * STAGE_BYTES;
-      mbar_expect_tx(&full[s], STAGE_BYTES);
-      tma_load_2d(&tm_a, &full[s], a_dst, kb * BK, row0);
-#pragma unroll
-      for (int ac = 0; ac < NB; ++ac) {
-        uint8_t* b_dst = a_dst + A_BYTES + ac * B_BYTES;
-        const int j = blockIdx.x * NB + ac;  // column block of accumulator ac
-        if (MODE == 1) {
-          const int gate_row = g * 2 * p.I + j * (BN / 2);
-          tma_load_2d(&tm_b, &full[s], b_dst, kb * BK, gate_row);
-          tma_load_2d(&tm_b, &full[s], b_dst + B_BYTES / 2, kb * BK, gate_row + p.I);
-        } else {
-          tma_load_2d(&tm_b, &full[s], b_dst, kb * BK, g * p.H + j * BN);
-        }
+      if (kb >= pre) {
+        mbar_expect_tx(&full[s], STAGE_BYTES);
+        load_b(kb, a_dst, &full[s]);
       }
+      tma_load_2d(&tm_a, &full[s], a_dst, kb * BK, row0);
       issued = kb + 1;
     }
   } else if (warp == 1 && lane == 0) {
@@ -251,7 +282,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   }
   tc_fence_after();
   __syncthreads();
-  if (!s_fail) {
+  if (!s_fail && !s_stale) {
     const int r = warp * 32 + lane;  // tile row = TMEM lane
     const uint32_t lane_base0 = tmem + ((uint32_t)(warp * 32) << 16);
     for (int ac = 0; ac < NB; ++ac) {
@@ -300,12 +331,17 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       }
     }
     }
-  } else if (warp == 0 && lane == 0) {
+  } else if (s_fail && warp == 0 && lane == 0) {
     // Drain: wait (bounded) for every load this CTA issued before its memory goes away.
     for (int kb = 0; kb < issued; ++kb) mbar_wait(&full[kb % STAGES], (kb / STAGES) & 1);
   }
+  if (MODE == 1 && p.tile_done) asm volatile("fence.proxy.async.global;" ::: "memory");  // h rows: read by TMA
   tc_fence_before();
   __syncthreads();
+  if (MODE == 1 && p.tile_done && threadIdx.x == 0) {  // early down: this CTA's h rows are written
+    __threadfence();
+    atomicAdd(p.tile_done + blockIdx.y, 1u);
+  }
   if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -396,18 +432,25 @@ cudaError_t launch_tc_prefill(const TcPrefillArgs& a, cudaStream_t st) {
   const int max_tiles = (Tk + BM - 1) / BM + a.G;
   // two accumulators per CTA where the column blocks pair up (I/128 and H/256 even)
   const int cb1 = a.I / (BN / 2), cb2 = a.H / BN;
+  const int gx1 = cb1 % 2 == 0 ? cb1 / 2 : cb1;
+  p.tile_done = a.tile_done;
+  p.tile_need = (uint32_t)gx1;
+  if (a.tile_done &&
+      (e = cudaMemsetAsync(a.tile_done, 0, sizeof(uint32_t) * (size_t)max_tiles, st)) != cudaSuccess)
+    return e;
   p.K = a.H;
   if (cb1 % 2 == 0)
-    tc_grouped_gemm<1, 2><<<dim3(cb1 / 2, max_tiles), 128, Ring<2>::kSmemBytes, st>>>(ta1, tb1, p);
+    tc_grouped_gemm<1, 2><<<dim3(gx1, max_tiles), 128, Ring<2>::kSmemBytes, st>>>(ta1, tb1, p);
   else
-    tc_grouped_gemm<1, 1><<<dim3(cb1, max_tiles), 128, Ring<1>::kSmemBytes, st>>>(ta1, tb1, p);
+    tc_grouped_gemm<1, 1><<<dim3(gx1, max_tiles), 128, Ring<1>::kSmemBytes, st>>>(ta1, tb1, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.K = a.I;
+  const bool early = a.tile_done != nullptr;
   if (cb2 % 2 == 0)
-    tc_grouped_gemm<2, 2><<<dim3(cb2 / 2, max_tiles), 128, Ring<2>::kSmemBytes, st>>>(ta2, tb2, p);
-  else
-    tc_grouped_gemm<2, 1><<<dim3(cb2, max_tiles), 128, Ring<1>::kSmemBytes, st>>>(ta2, tb2, p);
-  return cudaGetLastError();
+    return launch_k(tc_grouped_gemm<2, 2>, dim3(cb2 / 2, max_tiles), dim3(128), Ring<2>::kSmemBytes, st, early, ta2,
+                    tb2, p);
+  return launch_k(tc_grouped_gemm<2, 1>, dim3(cb2, max_tiles), dim3(128), Ring<1>::kSmemBytes, st, early, ta2, tb2,
+                  p);
 }
 
 }  // namespace moe

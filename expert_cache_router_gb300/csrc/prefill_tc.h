@@ -15,6 +15,11 @@ struct TcGemmArgs {
   uint16_t* hp;            // [Tk, I] bf16 (gate/up output)
   float* y;                // [Tk, H] fp32, by pair (down output)
   uint32_t* status;
+  // Early down: gate/up CTAs count themselves into tile_done[tile] once their h rows
+  // are written; a down CTA starts under the gate/up launch and loads its tile's h
+  // rows once the count reaches tile_need. nullptr: the down launch follows gate/up.
+  uint32_t* tile_done;
+  uint32_t tile_need;
 };
 
 struct TcPrefillArgs {
@@ -31,6 +36,7 @@ struct TcPrefillArgs {
   uint16_t* hp;            // [Tk, I] scratch
   float* y;                // [Tk, H]
   uint32_t* status;
+  uint32_t* tile_done;     // [ceil(Tk/128) + G] scratch, zeroed here each call; nullptr: no early down
 };
 
 bool tc_gemm_supported(int H, int I);

@@ -97,3 +97,60 @@ def test_early_down_equals_full_wait(dev, stacks, monkeypatch, case):
         assert res["0"][1][key] == res["1"][1][key], (name, key)
     if "spills" in name:
         assert res["1"][1]["spills"] > 0, name
+
+
+# ------------------------------------------------------------------ prefill
+def _prefill(h, st, dev, T, layers):
+    """One staged call of T tokens per layer; returns the outputs and the stats."""
+    c = st.cfg
+    out = torch.empty((layers, T, c.hidden), dtype=torch.int16, device=dev)
+    for l in range(layers):
+        h.decode_layer(l, _bits(st.x[0, l, :T]).to(dev), T, out[l])
+    torch.cuda.synchronize()
+    return _u16(out), h.get_stats()
+
+
+PREFILL_CASES = [
+    # (name, stack kind, T, slots): every call touches more distinct experts than slots, so it stages
+    ("bf16 T48 S4", "bf16", 48, 4),
+    ("fp8+shared T48", "fp8", 48, None),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+def test_prefill_early_down_equals_full_wait(dev, monkeypatch, case):
+    """The tensor-core prefill GEMMs with the down launch started under the gate/up
+    launch (per-tile counts) write the same bits as with the down launch after it."""
+    name, kind, T, S = case
+    st = (Stack(TINY, num_layers=2, tokens=1, batch=T, stream=5) if kind == "bf16"
+          else Fp8Stack(TINY_FP8, tokens=1, batch=T, stream=5))
+    layers = st.cfg.num_layers
+    res = {}
+    for early in ("0", "1"):
+        monkeypatch.setenv("MOE_OFFLOAD_EARLY_DOWN", early)
+        h = st.handle(torch, dev, num_slots=S)
+        try:
+            res[early] = _prefill(h, st, dev, T, layers)
+        finally:
+            h.close()
+        assert res[early][1]["device_status"] == 0, name
+        assert res[early][1]["staged_calls"] == layers, name
+    assert np.array_equal(res["0"][0], res["1"][0]), name
+
+
+def test_prefill_early_down_full_size_qwen3_30b_a3b(dev, monkeypatch):
+    """A 2048-token prompt on one full Qwen3-30B-A3B layer (hundreds of 128-row tiles,
+    so down CTAs start while gate/up tiles are still running): same bits either way."""
+    from workload import QWEN3_30B_A3B
+    st = Stack(QWEN3_30B_A3B, num_layers=1, tokens=1, batch=2048, stream=2)
+    res = {}
+    for early in ("0", "1"):
+        monkeypatch.setenv("MOE_OFFLOAD_EARLY_DOWN", early)
+        h = st.handle(torch, dev)
+        try:
+            res[early] = _prefill(h, st, dev, 2048, 1)
+        finally:
+            h.close()
+        assert res[early][1]["device_status"] == 0
+        assert res[early][1]["staged_calls"] == 1
+    assert np.array_equal(res["0"][0], res["1"][0])
