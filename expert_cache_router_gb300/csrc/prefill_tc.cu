@@ -4,7 +4,9 @@
 // of the pairs are gathered in bucket order into Xp [Tk, H]. One CTA computes a
 // 128-row tile of one bucket against one column block of that bucket's expert:
 //   gate/up:  Xp[128 x H] . [W1 rows n..n+128 ; W3 rows n..n+128]^T -> TMEM
-//             [128 x 256] fp32, epilogue h = silu(g) * u -> Hp (bf16, bucket order)
+//             [128 x 256] fp32, epilogue h = silu(g) * u -> Hp (bf16, bucket order);
+//             with two accumulators, W1 rows n..n+256 into one and W3 rows n..n+256
+//             into the other (each weight box 256 contiguous rows)
 //   down:     Hp[128 x I] . W2[rows n..n+256]^T -> TMEM [128 x 256] fp32,
 //             epilogue writes y of each pair (fp32) for the rank-order combine
 // ("MoE expert offload" page, "How it works", Prefill: the unmodified GEMM runs
@@ -28,12 +30,14 @@
 // after every gate/up CTA has started, so a waiting down CTA never keeps a
 // producer off the GPU.
 //
-// Warp roles (4 warps): warp 0 allocates TMEM and, one lane, issues the TMA
+// Warp roles (16 warps): warp 0 allocates TMEM and, one lane, issues the TMA
 // loads of a shared-memory ring (8 stages for NB = 1, 5 stages of NB weight
 // tiles for NB = 2, K = 32 each); warp 1, one lane, issues tcgen05.mma (M=128, N=256, K=16,
 // bf16 in, fp32 accumulate; NB per K step) and commits each stage back to the
-// producer; all 4 warps read the accumulators with tcgen05.ld (warp w owns
-// TMEM lanes 32w..32w+31 = tile rows) for the epilogue. Every wait is bounded:
+// producer; all 16 warps read the accumulators with tcgen05.ld for the epilogue
+// (warp w reads TMEM lanes 32(w%4)..32(w%4)+31 = tile rows, and the w/4-th quarter
+// of the columns), so the epilogue, which runs while the SM's tensor core and
+// copies are idle, takes a quarter of the time it takes with 4 warps. Every wait is bounded:
 // a wait that runs out sets a status bit and the CTA drains its own copies
 // (again bounded), frees TMEM and returns.
 #include <cuda.h>
@@ -61,6 +65,8 @@ struct Ring {
 };
 static_assert(Ring<2>::kSmemBytes <= 227 * 1024 && Ring<1>::kSmemBytes <= 227 * 1024, "GEMM shared memory");
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kGemmThreads = 512;                // 16 warps
+constexpr int kColParts = kGemmThreads / 128;    // epilogue warps per TMEM lane quadrant
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -158,10 +164,12 @@ __device__ bool tile_of(const int32_t* counts, const int32_t* offsets, const int
 }
 
 // MODE 1: gate/up + SiLU epilogue into Hp. MODE 2: down projection into Y by pair.
-// Column block j = blockIdx.x * NB + a of accumulator a: gate rows j*128.. and up
-// rows I + j*128.. (MODE 1), or output columns j*256.. (MODE 2).
+// MODE 1 with NB = 2: gate rows blockIdx.x*256.. in accumulator 0 and the matching
+// up rows I + blockIdx.x*256.. in accumulator 1; with NB = 1: gate rows j*128.. and up
+// rows I + j*128.. (j = blockIdx.x) in one accumulator. MODE 2: output columns
+// j*256.. in accumulator a, j = blockIdx.x * NB + a.
 template <int MODE, int NB>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, TcGemmArgs p) {
   constexpr int STAGES = Ring<NB>::kStages;
   constexpr int STAGE_BYTES = Ring<NB>::kStageBytes;
@@ -215,7 +223,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       for (int ac = 0; ac < NB; ++ac) {
         uint8_t* b_dst = a_dst + A_BYTES + ac * B_BYTES;
         const int j = blockIdx.x * NB + ac;  // column block of accumulator ac
-        if (MODE == 1) {
+        if (MODE == 1 && NB == 2) {  // accumulator 0: 256 gate rows, 1: the matching 256 up rows
+          tma_load_2d(tmb, bar, b_dst, kb * BK, g * 2 * p.I + (ac ? p.I : 0) + blockIdx.x * BN);
+        } else if (MODE == 1) {  // one accumulator: 128 gate rows, then the matching 128 up rows
           const int gate_row = g * 2 * p.I + j * (BN / 2);
           tma_load_2d(tmb, bar, b_dst, kb * BK, gate_row);
           tma_load_2d(tmb, bar, b_dst + B_BYTES / 2, kb * BK, gate_row + p.I);
@@ -283,17 +293,23 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   tc_fence_after();
   __syncthreads();
   if (!s_fail && !s_stale) {
-    const int r = warp * 32 + lane;  // tile row = TMEM lane
-    const uint32_t lane_base0 = tmem + ((uint32_t)(warp * 32) << 16);
-    for (int ac = 0; ac < NB; ++ac) {
+    const int quad = warp & 3, part = warp >> 2;  // TMEM lane quadrant, quarter of the columns
+    const int r = quad * 32 + lane;                // tile row = TMEM lane
+    const uint32_t lane_base0 = tmem + ((uint32_t)(quad * 32) << 16);
+    // gate/up with two accumulators: gate column c in accumulator 0, up column c in 1
+    for (int ac = 0; ac < (MODE == 1 && NB == 2 ? 1 : NB); ++ac) {
     const uint32_t lane_base = lane_base0 + (uint32_t)(ac * BN);
     const int j = blockIdx.x * NB + ac;
     if (MODE == 1) {
-      const int col0 = j * (BN / 2);
-      for (int c = 0; c < BN / 2; c += 32) {
+      constexpr int kCols = NB == 2 ? BN : BN / 2;  // h columns of this CTA
+      constexpr int kUp = NB == 2 ? BN : BN / 2;    // TMEM column offset of the up values
+      constexpr int kPart = kCols / kColParts;
+      static_assert(kPart % 32 == 0, "epilogue column split");
+      const int col0 = NB == 2 ? blockIdx.x * BN : j * (BN / 2);
+      for (int c = part * kPart; c < (part + 1) * kPart; c += 32) {
         uint32_t gv[32], uv[32];
         tmem_ld32(lane_base + c, gv);
-        tmem_ld32(lane_base + BN / 2 + c, uv);
+        tmem_ld32(lane_base + kUp + c, uv);
         tmem_wait_ld();
         if (r < rows) {
           uint32_t packed[16];
@@ -317,7 +333,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     } else {
       const int col0 = j * BN;
       const int pair = r < rows ? p.perm[row0 + r] : 0;
-      for (int c = 0; c < BN; c += 32) {
+      constexpr int kPart = BN / kColParts;
+      static_assert(kPart % 32 == 0, "epilogue column split");
+      for (int c = part * kPart; c < (part + 1) * kPart; c += 32) {
         uint32_t v[32];
         tmem_ld32(lane_base + c, v);
         tmem_wait_ld();
@@ -415,7 +433,10 @@ cudaError_t launch_tc_prefill(const TcPrefillArgs& a, cudaStream_t st) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   CUtensorMap ta1, tb1, ta2, tb2;
   if ((e = make_map(&ta1, a.xp, (uint64_t)Tk, (uint64_t)a.H, BM)) != cudaSuccess) return e;
-  if ((e = make_map(&tb1, a.w13, (uint64_t)a.G * 2 * a.I, (uint64_t)a.H, BN / 2)) != cudaSuccess) return e;
+  // gate/up weight boxes: 256 rows (two accumulators, gate block and up block) or 128 (one)
+  const bool pair1 = (a.I / (BN / 2)) % 2 == 0;
+  if ((e = make_map(&tb1, a.w13, (uint64_t)a.G * 2 * a.I, (uint64_t)a.H, pair1 ? BN : BN / 2)) != cudaSuccess)
+    return e;
   if ((e = make_map(&ta2, a.hp, (uint64_t)Tk, (uint64_t)a.I, BM)) != cudaSuccess) return e;
   if ((e = make_map(&tb2, a.w2, (uint64_t)a.G * a.H, (uint64_t)a.I, BN)) != cudaSuccess) return e;
   TcGemmArgs p{};
@@ -440,16 +461,16 @@ cudaError_t launch_tc_prefill(const TcPrefillArgs& a, cudaStream_t st) {
     return e;
   p.K = a.H;
   if (cb1 % 2 == 0)
-    tc_grouped_gemm<1, 2><<<dim3(gx1, max_tiles), 128, Ring<2>::kSmemBytes, st>>>(ta1, tb1, p);
+    tc_grouped_gemm<1, 2><<<dim3(gx1, max_tiles), kGemmThreads, Ring<2>::kSmemBytes, st>>>(ta1, tb1, p);
   else
-    tc_grouped_gemm<1, 1><<<dim3(gx1, max_tiles), 128, Ring<1>::kSmemBytes, st>>>(ta1, tb1, p);
+    tc_grouped_gemm<1, 1><<<dim3(gx1, max_tiles), kGemmThreads, Ring<1>::kSmemBytes, st>>>(ta1, tb1, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.K = a.I;
   const bool early = a.tile_done != nullptr;
   if (cb2 % 2 == 0)
-    return launch_k(tc_grouped_gemm<2, 2>, dim3(cb2 / 2, max_tiles), dim3(128), Ring<2>::kSmemBytes, st, early, ta2,
+    return launch_k(tc_grouped_gemm<2, 2>, dim3(cb2 / 2, max_tiles), dim3(kGemmThreads), Ring<2>::kSmemBytes, st, early, ta2,
                     tb2, p);
-  return launch_k(tc_grouped_gemm<2, 1>, dim3(cb2, max_tiles), dim3(128), Ring<1>::kSmemBytes, st, early, ta2, tb2,
+  return launch_k(tc_grouped_gemm<2, 1>, dim3(cb2, max_tiles), dim3(kGemmThreads), Ring<1>::kSmemBytes, st, early, ta2, tb2,
                   p);
 }
 
