@@ -146,6 +146,29 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// Epilogue transpose tile: 32 rows of up to 32 words per warp, row stride 33 words
+// (writes by row and reads by column are both free of bank conflicts).
+constexpr int kTileStride = 33;
+static_assert(kGemmThreads / 32 * 32 * kTileStride * 4 <= 5 * (BM * BK * 2 + 2 * BN * BK * 2), "epilogue tiles fit the ring");
+
+// Stores a warp's transpose tile (32 rows x W words, W = 16 or 32) row segment by row
+// segment: W/4 lanes per row, 16 bytes each, 128/W rows per instruction. dst(rr) gives
+// the first word of row rr's segment in global memory, or nullptr for a row past the tile.
+// Every lane calls dst for every iteration (it may hold a warp shuffle).
+template <int W, typename Dst>
+__device__ __forceinline__ void store_rows(const uint32_t* tile, int lane, Dst dst) {
+  constexpr int kLanesPerRow = W / 4, kRowsPerStep = 32 / kLanesPerRow;
+#pragma unroll
+  for (int it = 0; it < 32 / kRowsPerStep; ++it) {
+    const int rr = it * kRowsPerStep + lane / kLanesPerRow;
+    const int w0 = (lane % kLanesPerRow) * 4;
+    const uint32_t* src = tile + rr * kTileStride + w0;
+    const uint4 v = make_uint4(src[0], src[1], src[2], src[3]);
+    uint32_t* d = dst(rr);
+    if (d) *reinterpret_cast<uint4*>(d + w0) = v;
+  }
+}
+
 // Tile t -> (bucket, first row of the tile in bucket order, valid rows).
 __device__ bool tile_of(const int32_t* counts, const int32_t* offsets, const int32_t* tiles, int G, int t,
                         int* g_out, int* row0, int* rows) {
@@ -293,9 +316,15 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   tc_fence_after();
   __syncthreads();
   if (!s_fail && !s_stale) {
+    // Epilogue. Each warp moves its 32 rows through a transpose tile in shared memory
+    // (the idle ring: every load it received was consumed by the MMAs), so that each
+    // store instruction writes four (or eight) row segments of 128 (64) bytes instead
+    // of 32 segments of 16 bytes.
     const int quad = warp & 3, part = warp >> 2;  // TMEM lane quadrant, quarter of the columns
     const int r = quad * 32 + lane;                // tile row = TMEM lane
     const uint32_t lane_base0 = tmem + ((uint32_t)(quad * 32) << 16);
+    uint32_t* tile = reinterpret_cast<uint32_t*>(smem) + warp * (32 * kTileStride);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     // gate/up with two accumulators: gate column c in accumulator 0, up column c in 1
     for (int ac = 0; ac < (MODE == 1 && NB == 2 ? 1 : NB); ++ac) {
     const uint32_t lane_base = lane_base0 + (uint32_t)(ac * BN);
@@ -303,49 +332,52 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     if (MODE == 1) {
       constexpr int kCols = NB == 2 ? BN : BN / 2;  // h columns of this CTA
       constexpr int kUp = NB == 2 ? BN : BN / 2;    // TMEM column offset of the up values
-      constexpr int kPart = kCols / kColParts;
-      static_assert(kPart % 32 == 0, "epilogue column split");
-      const int col0 = NB == 2 ? blockIdx.x * BN : j * (BN / 2);
-      for (int c = part * kPart; c < (part + 1) * kPart; c += 32) {
+      constexpr int kPart = kCols / kColParts;      // this warp's h columns: 64 or 32
+      constexpr int kWords = kPart / 2;             // bf16 pairs per row
+      static_assert(kPart % 32 == 0 && (kWords == 16 || kWords == 32), "epilogue column split");
+      const int col0 = (NB == 2 ? blockIdx.x * BN : j * (BN / 2)) + part * kPart;
+#pragma unroll 1
+      for (int c = 0; c < kPart; c += 32) {
         uint32_t gv[32], uv[32];
-        tmem_ld32(lane_base + c, gv);
-        tmem_ld32(lane_base + kUp + c, uv);
+        tmem_ld32(lane_base + part * kPart + c, gv);
+        tmem_ld32(lane_base + kUp + part * kPart + c, uv);
         tmem_wait_ld();
-        if (r < rows) {
-          uint32_t packed[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float h2[2];
+        for (int q = 0; q < 16; ++q) {
+          float h2[2];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const float gs = __uint_as_float(gv[2 * j + q]), us = __uint_as_float(uv[2 * j + q]);
-              h2[q] = gs / (1.0f + expf(-gs)) * us;
-            }
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(h2[0], h2[1]);
-            packed[j] = *reinterpret_cast<const uint32_t*>(&b2);
+          for (int e = 0; e < 2; ++e) {
+            const float gs = __uint_as_float(gv[2 * q + e]), us = __uint_as_float(uv[2 * q + e]);
+            h2[e] = gs / (1.0f + expf(-gs)) * us;
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.hp + (size_t)(row0 + r) * p.I + col0 + c);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(h2[0], h2[1]);
+          tile[lane * kTileStride + c / 2 + q] = *reinterpret_cast<const uint32_t*>(&b2);
         }
       }
+      __syncwarp();
+      store_rows<kWords>(tile, lane, [&](int rr) -> uint32_t* {
+        const int row = quad * 32 + rr;
+        return row < rows ? reinterpret_cast<uint32_t*>(p.hp + (size_t)(row0 + row) * p.I + col0) : nullptr;
+      });
+      __syncwarp();
     } else {
       const int col0 = j * BN;
       const int pair = r < rows ? p.perm[row0 + r] : 0;
       constexpr int kPart = BN / kColParts;
       static_assert(kPart % 32 == 0, "epilogue column split");
+#pragma unroll 1
       for (int c = part * kPart; c < (part + 1) * kPart; c += 32) {
         uint32_t v[32];
         tmem_ld32(lane_base + c, v);
         tmem_wait_ld();
-        if (r < rows) {
-          float4* dst = reinterpret_cast<float4*>(p.y + (size_t)pair * p.H + col0 + c);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-        }
+        for (int q = 0; q < 32; ++q) tile[lane * kTileStride + q] = v[q];
+        __syncwarp();
+        store_rows<32>(tile, lane, [&](int rr) -> uint32_t* {
+          const int pr = __shfl_sync(0xffffffffu, pair, rr);
+          return quad * 32 + rr < rows ? reinterpret_cast<uint32_t*>(p.y + (size_t)pr * p.H + col0 + c) : nullptr;
+        });
+        __syncwarp();
       }
     }
     }
