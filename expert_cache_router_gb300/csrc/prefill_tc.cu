@@ -4,9 +4,7 @@
 // of the pairs are gathered in bucket order into Xp [Tk, H]. One CTA computes a
 // 128-row tile of one bucket against one column block of that bucket's expert:
 //   gate/up:  Xp[128 x H] . [W1 rows n..n+128 ; W3 rows n..n+128]^T -> TMEM
-//             [128 x 256] fp32, epilogue h = silu(g) * u -> Hp (bf16, bucket order);
-//             with two accumulators, W1 rows n..n+256 into one and W3 rows n..n+256
-//             into the other (each weight box 256 contiguous rows)
+//             [128 x 256] fp32, epilogue h = silu(g) * u -> Hp (bf16, bucket order)
 //   down:     Hp[128 x I] . W2[rows n..n+256]^T -> TMEM [128 x 256] fp32,
 //             epilogue writes y of each pair (fp32) for the rank-order combine
 // ("MoE expert offload" page, "How it works", Prefill: the unmodified GEMM runs
@@ -14,12 +12,11 @@
 // the end of its bucket are computed and discarded; every output row depends
 // only on its own input row, so the bucket order never changes a result.
 //
-// A CTA holds NB accumulators of 256 fp32 columns (NB = 2 when the column
-// blocks pair up: 512 TMEM columns), so that each x (or h) tile it streams
-// feeds NB column blocks and the tile is read from memory 1/NB as often. At
-// prefill sizes (about 128 rows per expert) the kernels are bound by the
-// weight bytes they stream, so the ring is made of small stages (K = 32,
-// 64-byte swizzle) to keep more bytes in flight per SM.
+// Two CTAs per SM (256 TMEM columns and a 96 KB ring each), so that one CTA's
+// epilogue, which leaves the tensor core and the copies idle, overlaps the other
+// CTA's main loop. At prefill sizes (about 128 rows per expert) the kernels are
+// bound by the bytes they stream; the ring is made of small stages (K = 32,
+// 64-byte swizzle).
 //
 // Early down: the down launch follows the gate/up launch under programmatic
 // dependent launch. Each gate/up CTA triggers it at its start and, once its h
@@ -30,14 +27,13 @@
 // after every gate/up CTA has started, so a waiting down CTA never keeps a
 // producer off the GPU.
 //
-// Warp roles (16 warps): warp 0 allocates TMEM and, one lane, issues the TMA
-// loads of a shared-memory ring (8 stages for NB = 1, 5 stages of NB weight
-// tiles for NB = 2, K = 32 each); warp 1, one lane, issues tcgen05.mma (M=128, N=256, K=16,
-// bf16 in, fp32 accumulate; NB per K step) and commits each stage back to the
-// producer; all 16 warps read the accumulators with tcgen05.ld for the epilogue
-// (warp w reads TMEM lanes 32(w%4)..32(w%4)+31 = tile rows, and the w/4-th quarter
-// of the columns), so the epilogue, which runs while the SM's tensor core and
-// copies are idle, takes a quarter of the time it takes with 4 warps. Every wait is bounded:
+// Warp roles (8 warps): warp 0 allocates TMEM and, one lane, issues the TMA
+// loads of a 4-stage shared-memory ring (K = 32 each); warp 1, one lane, issues
+// tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate) and commits each
+// stage back to the producer; all 8 warps read the accumulator with tcgen05.ld
+// for the epilogue (warp w reads TMEM lanes 32(w%4)..32(w%4)+31 = tile rows and
+// the w/4-th half of the columns) and move their rows through a transpose tile
+// in the idle ring, so that stores write whole row segments. Every wait is bounded:
 // a wait that runs out sets a status bit and the CTA drains its own copies
 // (again bounded), frees TMEM and returns.
 #include <cuda.h>
@@ -52,21 +48,19 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;        // tile rows (pairs)
-constexpr int BN = 256;        // columns of one accumulator
+constexpr int BN = 256;        // accumulator columns
 constexpr int BK = 32;         // K per stage: one 64-byte swizzle row of bf16
 constexpr int A_BYTES = BM * BK * 2;     // 8 KB
-constexpr int B_BYTES = BN * BK * 2;     // 16 KB per accumulator
-template <int NB>
-struct Ring {
-  static constexpr int kStages = NB == 1 ? 8 : 5;
-  static constexpr int kStageBytes = A_BYTES + NB * B_BYTES;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
-  static constexpr uint32_t kTmemCols = 256u * NB;
-};
-static_assert(Ring<2>::kSmemBytes <= 227 * 1024 && Ring<1>::kSmemBytes <= 227 * 1024, "GEMM shared memory");
-constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr int kGemmThreads = 512;                // 16 warps
+constexpr int B_BYTES = BN * BK * 2;     // 16 KB
+constexpr int kStages = 4;
+constexpr int kStageBytes = A_BYTES + B_BYTES;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;  // ring, 1 KB alignment slack, barriers
+constexpr uint32_t kTmemCols = BN;
+constexpr int kGemmThreads = 256;                // 8 warps
 constexpr int kColParts = kGemmThreads / 128;    // epilogue warps per TMEM lane quadrant
+constexpr int kCtasPerSm = 2;
+static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024 && kCtasPerSm * kTmemCols <= 512, "two CTAs per SM");
+constexpr uint32_t kWaitLimit = 1u << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -149,7 +143,7 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 // Epilogue transpose tile: 32 rows of up to 32 words per warp, row stride 33 words
 // (writes by row and reads by column are both free of bank conflicts).
 constexpr int kTileStride = 33;
-static_assert(kGemmThreads / 32 * 32 * kTileStride * 4 <= 5 * (BM * BK * 2 + 2 * BN * BK * 2), "epilogue tiles fit the ring");
+static_assert(kGemmThreads / 32 * 32 * kTileStride * 4 <= kStages * kStageBytes, "epilogue tiles fit the ring");
 
 // Stores a warp's transpose tile (32 rows x W words, W = 16 or 32) row segment by row
 // segment: W/4 lanes per row, 16 bytes each, 128/W rows per instruction. dst(rr) gives
@@ -186,28 +180,23 @@ __device__ bool tile_of(const int32_t* counts, const int32_t* offsets, const int
   return *rows > 0;
 }
 
-// MODE 1: gate/up + SiLU epilogue into Hp. MODE 2: down projection into Y by pair.
-// MODE 1 with NB = 2: gate rows blockIdx.x*256.. in accumulator 0 and the matching
-// up rows I + blockIdx.x*256.. in accumulator 1; with NB = 1: gate rows j*128.. and up
-// rows I + j*128.. (j = blockIdx.x) in one accumulator. MODE 2: output columns
-// j*256.. in accumulator a, j = blockIdx.x * NB + a.
-template <int MODE, int NB>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// MODE 1: gate/up + SiLU epilogue into Hp; column block j = blockIdx.x: gate rows
+// j*128.. and the matching up rows I + j*128.. in one accumulator (h columns
+// j*128..). MODE 2: down projection into Y by pair, output columns j*256...
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, TcGemmArgs p) {
-  constexpr int STAGES = Ring<NB>::kStages;
-  constexpr int STAGE_BYTES = Ring<NB>::kStageBytes;
-  constexpr uint32_t kTmemCols = Ring<NB>::kTmemCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* empty = full + STAGES;
-  uint64_t* done = empty + STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* done = empty + kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   __shared__ int s_fail;
   __shared__ int s_stale;  // early down: the tile's h rows did not arrive in time (no output written)
 
   if (MODE == 1) pdl_trigger();  // the down launch may start once every gate/up CTA has started
-  // blockIdx.x: column block pair, blockIdx.y: row tile. The CTAs of one tile are adjacent in
+  // blockIdx.x: column block, blockIdx.y: row tile. The CTAs of one tile are adjacent in
   // launch order, so they run together and its x (or h) tile is read from DRAM once and then
   // from L2; so are the tiles of one bucket, which share its weights.
   int g, row0, rows;
@@ -218,7 +207,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   if (threadIdx.x == 0) {
     s_fail = 0;
     s_stale = 0;
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -239,30 +228,24 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 
   int issued = 0;  // stages the producer loaded (for the drain on failure)
   if (warp == 0 && lane == 0) {
-    // TMA producer. Stage kb: the A tile (x or h rows) and NB weight tiles.
+    // TMA producer. Stage kb: the A tile (x or h rows) and the weight tile.
     const CUtensorMap* tmb = &tm_b;
     auto load_b = [&](int kb, uint8_t* a_dst, uint64_t* bar) {
-#pragma unroll
-      for (int ac = 0; ac < NB; ++ac) {
-        uint8_t* b_dst = a_dst + A_BYTES + ac * B_BYTES;
-        const int j = blockIdx.x * NB + ac;  // column block of accumulator ac
-        if (MODE == 1 && NB == 2) {  // accumulator 0: 256 gate rows, 1: the matching 256 up rows
-          tma_load_2d(tmb, bar, b_dst, kb * BK, g * 2 * p.I + (ac ? p.I : 0) + blockIdx.x * BN);
-        } else if (MODE == 1) {  // one accumulator: 128 gate rows, then the matching 128 up rows
-          const int gate_row = g * 2 * p.I + j * (BN / 2);
-          tma_load_2d(tmb, bar, b_dst, kb * BK, gate_row);
-          tma_load_2d(tmb, bar, b_dst + B_BYTES / 2, kb * BK, gate_row + p.I);
-        } else {
-          tma_load_2d(tmb, bar, b_dst, kb * BK, g * p.H + j * BN);
-        }
+      uint8_t* b_dst = a_dst + A_BYTES;
+      if (MODE == 1) {
+        const int gate_row = g * 2 * p.I + blockIdx.x * (BN / 2);
+        tma_load_2d(tmb, bar, b_dst, kb * BK, gate_row);
+        tma_load_2d(tmb, bar, b_dst + B_BYTES / 2, kb * BK, gate_row + p.I);
+      } else {
+        tma_load_2d(tmb, bar, b_dst, kb * BK, g * p.H + blockIdx.x * BN);
       }
     };
     // Early down: the weight tiles of the first stages do not depend on the gate/up
     // launch and go out at once; the h tiles follow once the tile's count is complete.
-    const int pre = (MODE == 2 && p.tile_done) ? min(nk, STAGES) : 0;
+    const int pre = (MODE == 2 && p.tile_done) ? min(nk, kStages) : 0;
     for (int kb = 0; kb < pre; ++kb) {
-      mbar_expect_tx(&full[kb], STAGE_BYTES);
-      load_b(kb, smem + kb * STAGE_BYTES, &full[kb]);
+      mbar_expect_tx(&full[kb], kStageBytes);
+      load_b(kb, smem + kb * kStageBytes, &full[kb]);
     }
     if (pre) {
       // On a timeout (status bit set) every stage is still loaded and consumed, so no
@@ -271,15 +254,15 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       asm volatile("fence.proxy.async.global;" ::: "memory");  // h rows were written by generic stores
     }
     for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      if (kb >= STAGES && !mbar_wait(&empty[s], ((kb / STAGES) - 1) & 1)) {
+      const int s = kb % kStages;
+      if (kb >= kStages && !mbar_wait(&empty[s], ((kb / kStages) - 1) & 1)) {
         atomicOr(p.status, kDevTimeout);
         s_fail = 1;
         break;
       }
-      uint8_t* a_dst = smem + s * STAGE_BYTES;
+      uint8_t* a_dst = smem + s * kStageBytes;
       if (kb >= pre) {
-        mbar_expect_tx(&full[s], STAGE_BYTES);
+        mbar_expect_tx(&full[s], kStageBytes);
         load_b(kb, a_dst, &full[s]);
       }
       tma_load_2d(&tm_a, &full[s], a_dst, kb * BK, row0);
@@ -289,20 +272,17 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     // MMA issuer
     constexpr uint32_t idesc = idesc_bf16(BM, BN);
     for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      if (!mbar_wait(&full[s], (kb / STAGES) & 1)) {
+      const int s = kb % kStages;
+      if (!mbar_wait(&full[s], (kb / kStages) & 1)) {
         atomicOr(p.status, kDevTimeout);
         s_fail = 1;
         break;
       }
       tc_fence_after();
-      const uint8_t* a = smem + s * STAGE_BYTES;
+      const uint8_t* a = smem + s * kStageBytes;
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk)
-#pragma unroll
-        for (int ac = 0; ac < NB; ++ac)
-          mma_bf16(tmem + (uint32_t)(ac * BN), sdesc(a + kk * 32), sdesc(a + A_BYTES + ac * B_BYTES + kk * 32), idesc,
-                   (kb > 0 || kk > 0) ? 1u : 0u);
+        mma_bf16(tmem, sdesc(a + kk * 32), sdesc(a + A_BYTES + kk * 32), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
       mma_commit(&empty[s]);
     }
     mma_commit(done);
@@ -318,29 +298,22 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   if (!s_fail && !s_stale) {
     // Epilogue. Each warp moves its 32 rows through a transpose tile in shared memory
     // (the idle ring: every load it received was consumed by the MMAs), so that each
-    // store instruction writes four (or eight) row segments of 128 (64) bytes instead
-    // of 32 segments of 16 bytes.
-    const int quad = warp & 3, part = warp >> 2;  // TMEM lane quadrant, quarter of the columns
+    // store instruction writes four row segments of 128 bytes instead of 32 segments
+    // of 16 bytes.
+    const int quad = warp & 3, part = warp >> 2;  // TMEM lane quadrant, half of the columns
     const int r = quad * 32 + lane;                // tile row = TMEM lane
-    const uint32_t lane_base0 = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     uint32_t* tile = reinterpret_cast<uint32_t*>(smem) + warp * (32 * kTileStride);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    // gate/up with two accumulators: gate column c in accumulator 0, up column c in 1
-    for (int ac = 0; ac < (MODE == 1 && NB == 2 ? 1 : NB); ++ac) {
-    const uint32_t lane_base = lane_base0 + (uint32_t)(ac * BN);
-    const int j = blockIdx.x * NB + ac;
     if (MODE == 1) {
-      constexpr int kCols = NB == 2 ? BN : BN / 2;  // h columns of this CTA
-      constexpr int kUp = NB == 2 ? BN : BN / 2;    // TMEM column offset of the up values
-      constexpr int kPart = kCols / kColParts;      // this warp's h columns: 64 or 32
-      constexpr int kWords = kPart / 2;             // bf16 pairs per row
-      static_assert(kPart % 32 == 0 && (kWords == 16 || kWords == 32), "epilogue column split");
-      const int col0 = (NB == 2 ? blockIdx.x * BN : j * (BN / 2)) + part * kPart;
+      constexpr int kPart = BN / 2 / kColParts;  // this warp's h columns (gate in 0..127, up in 128..255)
+      static_assert(kPart == 64, "epilogue column split");
+      const int col0 = blockIdx.x * (BN / 2) + part * kPart;
 #pragma unroll 1
       for (int c = 0; c < kPart; c += 32) {
         uint32_t gv[32], uv[32];
         tmem_ld32(lane_base + part * kPart + c, gv);
-        tmem_ld32(lane_base + kUp + part * kPart + c, uv);
+        tmem_ld32(lane_base + BN / 2 + part * kPart + c, uv);
         tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -348,20 +321,19 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const float gs = __uint_as_float(gv[2 * q + e]), us = __uint_as_float(uv[2 * q + e]);
-            h2[e] = gs / (1.0f + expf(-gs)) * us;
+            h2[e] = __fdividef(gs, 1.0f + __expf(-gs)) * us;  // silu(g) * u; h is rounded to bf16 next
           }
           const __nv_bfloat162 b2 = __floats2bfloat162_rn(h2[0], h2[1]);
           tile[lane * kTileStride + c / 2 + q] = *reinterpret_cast<const uint32_t*>(&b2);
         }
       }
       __syncwarp();
-      store_rows<kWords>(tile, lane, [&](int rr) -> uint32_t* {
+      store_rows<kPart / 2>(tile, lane, [&](int rr) -> uint32_t* {
         const int row = quad * 32 + rr;
         return row < rows ? reinterpret_cast<uint32_t*>(p.hp + (size_t)(row0 + row) * p.I + col0) : nullptr;
       });
-      __syncwarp();
     } else {
-      const int col0 = j * BN;
+      const int col0 = blockIdx.x * BN;
       const int pair = r < rows ? p.perm[row0 + r] : 0;
       constexpr int kPart = BN / kColParts;
       static_assert(kPart % 32 == 0, "epilogue column split");
@@ -380,10 +352,9 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         __syncwarp();
       }
     }
-    }
   } else if (s_fail && warp == 0 && lane == 0) {
     // Drain: wait (bounded) for every load this CTA issued before its memory goes away.
-    for (int kb = 0; kb < issued; ++kb) mbar_wait(&full[kb % STAGES], (kb / STAGES) & 1);
+    for (int kb = 0; kb < issued; ++kb) mbar_wait(&full[kb % kStages], (kb / kStages) & 1);
   }
   if (MODE == 1 && p.tile_done) asm volatile("fence.proxy.async.global;" ::: "memory");  // h rows: read by TMA
   tc_fence_before();
@@ -444,16 +415,9 @@ bool tc_gemm_supported(int H, int I) { return H % BN == 0 && I % (BN / 2) == 0 &
 int tc_gemm_tile_rows() { return BM; }
 
 cudaError_t tc_gemm_init_attributes() {
-  cudaError_t e = cudaSuccess;
-  for (cudaError_t r : {cudaFuncSetAttribute(tc_grouped_gemm<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Ring<1>::kSmemBytes),
-                        cudaFuncSetAttribute(tc_grouped_gemm<1, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Ring<2>::kSmemBytes),
-                        cudaFuncSetAttribute(tc_grouped_gemm<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Ring<1>::kSmemBytes),
-                        cudaFuncSetAttribute(tc_grouped_gemm<2, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Ring<2>::kSmemBytes)})
-    if (e == cudaSuccess) e = r;
+  cudaError_t e = cudaFuncSetAttribute(tc_grouped_gemm<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_grouped_gemm<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   return e;
 }
 
@@ -465,10 +429,8 @@ cudaError_t launch_tc_prefill(const TcPrefillArgs& a, cudaStream_t st) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   CUtensorMap ta1, tb1, ta2, tb2;
   if ((e = make_map(&ta1, a.xp, (uint64_t)Tk, (uint64_t)a.H, BM)) != cudaSuccess) return e;
-  // gate/up weight boxes: 256 rows (two accumulators, gate block and up block) or 128 (one)
-  const bool pair1 = (a.I / (BN / 2)) % 2 == 0;
-  if ((e = make_map(&tb1, a.w13, (uint64_t)a.G * 2 * a.I, (uint64_t)a.H, pair1 ? BN : BN / 2)) != cudaSuccess)
-    return e;
+  // gate/up weight boxes: 128 gate rows and the matching 128 up rows
+  if ((e = make_map(&tb1, a.w13, (uint64_t)a.G * 2 * a.I, (uint64_t)a.H, BN / 2)) != cudaSuccess) return e;
   if ((e = make_map(&ta2, a.hp, (uint64_t)Tk, (uint64_t)a.I, BM)) != cudaSuccess) return e;
   if ((e = make_map(&tb2, a.w2, (uint64_t)a.G * a.H, (uint64_t)a.I, BN)) != cudaSuccess) return e;
   TcGemmArgs p{};
@@ -483,27 +445,18 @@ cudaError_t launch_tc_prefill(const TcPrefillArgs& a, cudaStream_t st) {
   p.y = a.y;
   p.status = a.status;
   const int max_tiles = (Tk + BM - 1) / BM + a.G;
-  // two accumulators per CTA where the column blocks pair up (I/128 and H/256 even)
-  const int cb1 = a.I / (BN / 2), cb2 = a.H / BN;
-  const int gx1 = cb1 % 2 == 0 ? cb1 / 2 : cb1;
+  const int cb1 = a.I / (BN / 2), cb2 = a.H / BN;  // column blocks of the two GEMMs
   p.tile_done = a.tile_done;
-  p.tile_need = (uint32_t)gx1;
+  p.tile_need = (uint32_t)cb1;
   if (a.tile_done &&
       (e = cudaMemsetAsync(a.tile_done, 0, sizeof(uint32_t) * (size_t)max_tiles, st)) != cudaSuccess)
     return e;
   p.K = a.H;
-  if (cb1 % 2 == 0)
-    tc_grouped_gemm<1, 2><<<dim3(gx1, max_tiles), kGemmThreads, Ring<2>::kSmemBytes, st>>>(ta1, tb1, p);
-  else
-    tc_grouped_gemm<1, 1><<<dim3(gx1, max_tiles), kGemmThreads, Ring<1>::kSmemBytes, st>>>(ta1, tb1, p);
+  tc_grouped_gemm<1><<<dim3(cb1, max_tiles), kGemmThreads, kSmemBytes, st>>>(ta1, tb1, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.K = a.I;
-  const bool early = a.tile_done != nullptr;
-  if (cb2 % 2 == 0)
-    return launch_k(tc_grouped_gemm<2, 2>, dim3(cb2 / 2, max_tiles), dim3(kGemmThreads), Ring<2>::kSmemBytes, st, early, ta2,
-                    tb2, p);
-  return launch_k(tc_grouped_gemm<2, 1>, dim3(cb2, max_tiles), dim3(kGemmThreads), Ring<1>::kSmemBytes, st, early, ta2, tb2,
-                  p);
+  return launch_k(tc_grouped_gemm<2>, dim3(cb2, max_tiles), dim3(kGemmThreads), kSmemBytes, st,
+                  a.tile_done != nullptr, ta2, tb2, p);
 }
 
 }  // namespace moe
