@@ -29,7 +29,7 @@ EXPORTS = [
     "moe_offload_read_route_counts", "moe_offload_plan_static", "moe_offload_set_placement",
     "moe_offload_read_prefetch", "moe_offload_read_slot",
     "moe_offload_read_slot_scales", "moe_offload_set_shared_expert", "moe_offload_reset",
-    "moe_offload_host_alloc", "moe_offload_host_free", "moe_offload_prefill_times",
+    "moe_offload_host_alloc", "moe_offload_host_free", "moe_offload_prefill_times", "moe_offload_prefill_gemm_ms",
     "moe_offload_device_bytes", "moe_offload_get_config", "moe_offload_read_routing",
     "moe_offload_host_read_gbs", "moe_offload_debug_wait", "moe_offload_trace_enable", "moe_offload_trace_read",
     "moe_offload_graph_create", "moe_offload_graph_launch",
@@ -121,6 +121,8 @@ def _declare(L):
     L.moe_offload_host_free.argtypes = [_vp]
     L.moe_offload_prefill_times.restype = _st
     L.moe_offload_prefill_times.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp]
+    L.moe_offload_prefill_gemm_ms.restype = _st
+    L.moe_offload_prefill_gemm_ms.argtypes = [_vp, _vp]
     L.moe_offload_device_bytes.restype = ctypes.c_size_t
     L.moe_offload_device_bytes.argtypes = [_vp]
     L.moe_offload_get_config.restype = _st

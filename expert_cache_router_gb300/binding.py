@@ -344,6 +344,12 @@ class MoeOffload:
         return dict(route=v[0].value, copy=v[1].value, gemm=v[2].value, combine=v[3].value,
                     staged=bool(staged.value))
 
+    def prefill_gemm_ms(self) -> float:
+        """Time (ms) of the last prefill call's two tensor-core GEMM launches alone."""
+        v = ctypes.c_float()
+        self._check(self._L.moe_offload_prefill_gemm_ms(self.h, ctypes.byref(v)))
+        return v.value
+
 
 class DecodeGraph:
     """A whole-stack decode step captured as one CUDA graph (moe_offload_graph_*).

@@ -1160,6 +1160,17 @@ void moe_offload_host_free(void* ptr) {
   if (ptr) cudaFreeHost(ptr);
 }
 
+moe_status_t moe_offload_prefill_gemm_ms(moe_offload_t h, float* gemm_kernels_ms) {
+  if (!h || !gemm_kernels_ms) return MOE_ERR_INVALID;
+  moe_status_t st = set_device(h);
+  if (st != MOE_OK) return st;
+  if (h->prefill.last_staged < 0) return fail(h, MOE_ERR_INVALID, "no prefill call on this handle yet");
+  if (!h->prefill.last_tc) return fail(h, MOE_ERR_INVALID, "the last prefill call did not run the tensor-core GEMMs");
+  cudaError_t e = prefill_gemm_ms(&h->prefill, gemm_kernels_ms);
+  if (e != cudaSuccess) return cuda_fail(h, e, "prefill GEMM events");
+  return MOE_OK;
+}
+
 moe_status_t moe_offload_prefill_times(moe_offload_t h, float* route_ms, float* copy_ms, float* gemm_ms,
                                        float* combine_ms, int* staged) {
   if (!h) return MOE_ERR_INVALID;

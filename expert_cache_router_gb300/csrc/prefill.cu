@@ -525,6 +525,7 @@ cudaError_t prefill_layer(PrefillState* ps, const PrefillLayer& pl, const uint16
     return e;
   }
   const bool tc = tc_gemm_supported(pl.H, pl.I);
+  ps->last_tc = tc ? 1 : 0;
   const int P = Tk + (stage && pl.shared ? T : 0);  // pairs: routed, then one shared-expert pair per token
   group_count_kernel<<<(P + 255) / 256, 256, 0, st>>>(gidx, P, G, ps->meta);
   group_scan_kernel<<<1, kMaxGroups, 0, st>>>(G, tc ? tc_gemm_tile_rows() : BM, ps->meta);
@@ -536,6 +537,8 @@ cudaError_t prefill_layer(PrefillState* ps, const PrefillLayer& pl, const uint16
     ta.tiles = ps->meta + kMetaTiles; ta.Tk = P; ta.k = pl.k; ta.Tr = Tk; ta.G = G; ta.H = pl.H; ta.I = pl.I;
     ta.w13 = base13; ta.w2 = base2; ta.xp = ps->xp; ta.hp = ps->hb; ta.y = ps->yb; ta.status = pl.status;
     ta.tile_done = pl.early_down ? ps->tile_done : nullptr;
+    ta.ev_gemm_begin = ps->ev[6];
+    ta.ev_gemm_end = ps->ev[7];
     if ((e = launch_tc_prefill(ta, st)) != cudaSuccess) { *why = "tensor-core grouped GEMM"; return e; }
   } else {
     // shapes the 128x256 tensor-core tiling does not cover: CUDA-core tiles
@@ -556,6 +559,12 @@ cudaError_t prefill_layer(PrefillState* ps, const PrefillLayer& pl, const uint16
   }
   cudaEventRecord(ps->ev[5], st);
   return cudaSuccess;
+}
+
+cudaError_t prefill_gemm_ms(PrefillState* ps, float* ms) {
+  if (ps->last_staged < 0 || !ps->last_tc) return cudaErrorInvalidValue;
+  cudaError_t e = cudaEventSynchronize(ps->ev[7]);
+  return e != cudaSuccess ? e : cudaEventElapsedTime(ms, ps->ev[6], ps->ev[7]);
 }
 
 cudaError_t prefill_times(PrefillState* ps, float* ms4, int* staged) {

@@ -35,9 +35,11 @@ struct PrefillState {
   cudaStream_t stage_stream = nullptr;        // speculative copies
   int* host_distinct = nullptr;   // pinned: distinct experts of the call
   size_t bytes = 0;
-  // events of the last call: route start, route end, copy start, copy end, GEMMs end, combine end
-  cudaEvent_t ev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  // events of the last call: route start, route end, copy start, copy end, GEMMs end, combine end,
+  // and (tensor-core path) before the gate/up launch and after the down launch
+  cudaEvent_t ev[8] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
   int last_staged = -1;           // 1 staged, 0 slot path, -1 no call yet
+  int last_tc = 0;                // the last call ran the tensor-core GEMMs
 };
 
 struct PrefillLayer {
@@ -83,6 +85,9 @@ cudaError_t prefill_layer(PrefillState* ps, const PrefillLayer& pl, const uint16
 void prefill_forget(PrefillState* ps);
 // Times of the last call (route, copy or staging, grouping + GEMMs, combine), in ms.
 cudaError_t prefill_times(PrefillState* ps, float* ms4, int* staged);
+// Time of the last call's two tensor-core GEMM launches, in ms (cudaErrorInvalidValue when
+// the last call did not run them).
+cudaError_t prefill_gemm_ms(PrefillState* ps, float* ms);
 void prefill_destroy(PrefillState* ps);
 
 }  // namespace moe

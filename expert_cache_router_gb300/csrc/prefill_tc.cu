@@ -452,11 +452,14 @@ cudaError_t launch_tc_prefill(const TcPrefillArgs& a, cudaStream_t st) {
       (e = cudaMemsetAsync(a.tile_done, 0, sizeof(uint32_t) * (size_t)max_tiles, st)) != cudaSuccess)
     return e;
   p.K = a.H;
+  if (a.ev_gemm_begin && (e = cudaEventRecord(a.ev_gemm_begin, st)) != cudaSuccess) return e;
   tc_grouped_gemm<1><<<dim3(cb1, max_tiles), kGemmThreads, kSmemBytes, st>>>(ta1, tb1, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.K = a.I;
-  return launch_k(tc_grouped_gemm<2>, dim3(cb2, max_tiles), dim3(kGemmThreads), kSmemBytes, st,
-                  a.tile_done != nullptr, ta2, tb2, p);
+  if ((e = launch_k(tc_grouped_gemm<2>, dim3(cb2, max_tiles), dim3(kGemmThreads), kSmemBytes, st,
+                    a.tile_done != nullptr, ta2, tb2, p)) != cudaSuccess)
+    return e;
+  return a.ev_gemm_end ? cudaEventRecord(a.ev_gemm_end, st) : cudaSuccess;
 }
 
 }  // namespace moe

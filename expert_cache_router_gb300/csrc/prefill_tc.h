@@ -37,6 +37,8 @@ struct TcPrefillArgs {
   float* y;                // [Tk, H]
   uint32_t* status;
   uint32_t* tile_done;     // [ceil(Tk/128) + G] scratch, zeroed here each call; nullptr: no early down
+  cudaEvent_t ev_gemm_begin;  // recorded before the gate/up launch (nullptr: none)
+  cudaEvent_t ev_gemm_end;    // recorded after the down launch (nullptr: none)
 };
 
 bool tc_gemm_supported(int H, int I);

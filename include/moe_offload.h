@@ -398,6 +398,16 @@ void moe_offload_host_free(void* ptr);
 moe_status_t moe_offload_prefill_times(moe_offload_t h, float* route_ms, float* copy_ms, float* gemm_ms,
                                        float* combine_ms, int* staged);
 
+/* Time of the two tensor-core grouped GEMM launches (gate/up + SiLU, then the
+ * down projection) of the handle's last prefill call, in milliseconds: from a
+ * CUDA event recorded before the gate/up launch to one recorded after the down
+ * launch, so bucketing and the row gather are not in it ("MoE expert offload"
+ * page, "How it works", Prefill: the GEMMs on the staged layer or the slot
+ * tensors). Synchronises on that call. MOE_ERR_INVALID before any prefill call,
+ * or when the last one ran the CUDA-core GEMMs (shapes the 128 x 256 tensor-core
+ * tiles do not cover: H not a multiple of 256 or I not a multiple of 128). */
+moe_status_t moe_offload_prefill_gemm_ms(moe_offload_t h, float* gemm_kernels_ms);
+
 /* Bytes of device memory the handle holds. */
 size_t moe_offload_device_bytes(moe_offload_t h);
 

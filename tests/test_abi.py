@@ -102,6 +102,7 @@ def test_null_handle_calls_are_rejected(lib):
     assert lib.moe_offload_debug_write_table(None, 0, 0, 0, 0) == C.MOE_ERR_INVALID
     assert lib.moe_offload_audit(None, 0, None) == C.MOE_ERR_INVALID
     assert lib.moe_offload_get_config(None, None, None) == C.MOE_ERR_INVALID
+    assert lib.moe_offload_prefill_gemm_ms(None, None) == C.MOE_ERR_INVALID
     assert lib.moe_offload_read_routing(None, None, None, None, 0, None) == C.MOE_ERR_INVALID
     assert lib.moe_offload_debug_wait(None, 0, 0) == C.MOE_ERR_INVALID
     assert lib.moe_offload_trace_enable(None, 1) == C.MOE_ERR_INVALID

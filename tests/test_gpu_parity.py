@@ -627,12 +627,14 @@ def test_prefill_full_size_qwen3_30b_a3b(dev):
         h.decode_layer(0, _bits(x).to(dev), T, out)
         torch.cuda.synchronize()
         times = h.prefill_times()
+        gemm_kernels = h.prefill_gemm_ms()
         stats = h.get_stats()
         gids, gw = _gpu_route(h, 0, x, dev)
     finally:
         h.close()
     assert times["staged"] and stats["staged_calls"] == 1 and stats["device_status"] == 0
     assert times["gemm"] > 0 and times["copy"] > 0
+    assert 0 < gemm_kernels <= times["gemm"]  # the GEMM launches alone, inside the bucketing + GEMM phase
     sample = np.arange(0, T, 97)
     check_layer(_u16(out)[sample], x[sample], st_.wr[0], st_.w13[0], st_.w2[0], c.top_k, True, gids[sample],
                 gw[sample])
