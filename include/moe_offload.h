@@ -153,7 +153,8 @@ int moe_offload_slots_auto(size_t free_bytes, size_t reserve_bytes, int num_laye
  * Environment read at create: MOE_OFFLOAD_AUDIT=1 (see moe_offload_audit),
  * MOE_OFFLOAD_PDL=0 (no programmatic dependent launch in the decode chain),
  * MOE_OFFLOAD_EARLY_DOWN=0 (a decode step's down launch waits for the whole
- * gate/up launch instead of per expert; outputs are identical either way),
+ * gate/up launch instead of per expert, and a prefill call's down GEMM for the
+ * whole gate/up GEMM instead of per row tile; outputs are identical either way),
  * MOE_OFFLOAD_PROFILE=1 (see moe_offload_profile_read), and
  * MOE_OFFLOAD_FAIL_ALLOC=n, host-side fault injection: the n-th device
  * allocation or host registration of create (from 0) fails with MOE_ERR_OOM
