@@ -640,6 +640,34 @@ def test_prefill_full_size_qwen3_30b_a3b(dev):
                 gw[sample])
 
 
+@pytest.mark.parametrize("T, S, staged", [(333, 25, True), (64, 128, False)])
+def test_prefill_ragged_and_slot_path_qwen3_30b_a3b(dev, T, S, staged):
+    """Tensor-core prefill on one full Qwen3-30B-A3B layer at a token count that leaves
+    every bucket's last 128-row tile ragged (T=333, staged), and on the slot path (S=128:
+    every distinct expert gets a slot, so the GEMMs read the slot tensors after the
+    ensure and miss copy); sampled rows, near-ties included, against the oracle on the
+    GPU's routing."""
+    st_ = Stack(QWEN3_30B_A3B, num_layers=1, tokens=1, batch=T, stream=6)
+    c = st_.cfg
+    h = st_.handle(torch, dev, num_slots=S)
+    try:
+        x = st_.x[0, 0, :T]
+        out = torch.empty((T, c.hidden), dtype=torch.int16, device=dev)
+        h.decode_layer(0, _bits(x).to(dev), T, out)
+        torch.cuda.synchronize()
+        times = h.prefill_times()
+        gemm_kernels = h.prefill_gemm_ms()
+        stats = h.get_stats()
+        gids, gw = _gpu_route(h, 0, x, dev)
+    finally:
+        h.close()
+    assert times["staged"] == staged and stats["device_status"] == 0
+    assert 0 < gemm_kernels <= times["gemm"]
+    sample = np.arange(0, T, 7)
+    check_layer(_u16(out)[sample], x[sample], st_.wr[0], st_.w13[0], st_.w2[0], c.top_k, True, gids[sample],
+                gw[sample])
+
+
 def test_prefill_speculative_staging_in_and_out_of_order(dev):
     """Layer l+1 is staged while layer l computes; calls in order, out of order,
     repeated and interleaved with decode calls all give the oracle's outputs,
