@@ -567,18 +567,23 @@ def decode_batch(P, cfg, B, xw, xt, xt_host, K, W, repeats, stream, full=True, s
         early = P.delta(moe.get_stats(), before16)["misses"]
         r["steady_misses"] = (r["stats"]["misses"] - early) / max(K - n0, 1)
     if e2e:
+        # as many passes as the device-timed value, median taken the same way
         xh = torch.from_numpy(xt_host.view(np.int16)).pin_memory()
         oh = torch.empty((K, L, B, H), dtype=torch.int16).pin_memory()
-        P.restart()
-        P.dist.barrier()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for t in range(K):
-            g_plain.launch_host(xh[t], oh[t], stream)
-        b.record(stream)
-        torch.cuda.synchronize()
-        r["e2e_secs"] = P.dist.max(a.elapsed_time(b) * 1e-3)
+        e2e_all = []
+        for _ in range(repeats):
+            P.restart()
+            P.dist.barrier()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for t in range(K):
+                g_plain.launch_host(xh[t], oh[t], stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            e2e_all.append(P.dist.max(a.elapsed_time(b) * 1e-3))
+        r["e2e_secs"] = sorted(e2e_all)[repeats // 2]
+        r["e2e_secs_all"] = e2e_all
     g_plain.close()
     return r
 
@@ -817,7 +822,11 @@ def run_ours(args, dist):
         nbytes = L * H * 2
         line["e2e"] = {"value": world * K / r1["e2e_secs"], "unit": "tok/s", "h2d_bytes_per_step": nbytes,
                        "d2h_bytes_per_step": nbytes,
-                       "path": "moe_offload_graph_launch_host: pinned host in, graph replay, pinned host out, per step"}
+                       "repeats": {"n": len(r1["e2e_secs_all"]),
+                                   "min": world * K / max(r1["e2e_secs_all"]),
+                                   "max": world * K / min(r1["e2e_secs_all"])},
+                       "path": "moe_offload_graph_launch_host: pinned host in, graph replay, pinned host out, per step; "
+                               "median of the passes, each from an empty slot table like the device-timed value"}
     if trace is not None:
         line["trace"] = trace
     if not args.no_prefill and cfg.num_experts > cfg.num_slots and not static:
