@@ -841,6 +841,8 @@ moe_status_t moe_offload_decode_layer(moe_offload_t h, int layer, const void* x,
   pl.status = h->status;
   pl.frozen = h->frozen[layer];
   pl.early_down = h->early_down;
+  pl.wait_ns = h->wait_ns;
+  pl.stall = h->stall;
   pl.layer = layer;
   pl.next_host_w13 = nullptr;
   pl.next_host_w2 = nullptr;

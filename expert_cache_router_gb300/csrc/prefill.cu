@@ -537,6 +537,8 @@ cudaError_t prefill_layer(PrefillState* ps, const PrefillLayer& pl, const uint16
     ta.tiles = ps->meta + kMetaTiles; ta.Tk = P; ta.k = pl.k; ta.Tr = Tk; ta.G = G; ta.H = pl.H; ta.I = pl.I;
     ta.w13 = base13; ta.w2 = base2; ta.xp = ps->xp; ta.hp = ps->hb; ta.y = ps->yb; ta.status = pl.status;
     ta.tile_done = pl.early_down ? ps->tile_done : nullptr;
+    ta.wait_ns = pl.wait_ns;
+    ta.stall = pl.stall;
     ta.ev_gemm_begin = ps->ev[6];
     ta.ev_gemm_end = ps->ev[7];
     if ((e = launch_tc_prefill(ta, st)) != cudaSuccess) { *why = "tensor-core grouped GEMM"; return e; }

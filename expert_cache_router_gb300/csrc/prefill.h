@@ -71,6 +71,8 @@ struct PrefillLayer {
   uint32_t* status;
   int frozen;  // the layer holds a static placement: always stage (its table takes no installs)
   int early_down;  // tensor-core GEMMs: the down launch starts under gate/up (per-tile counts)
+  unsigned long long wait_ns;  // bound of that per-tile wait (0: the default)
+  int stall;                   // debug: the per-tile wait targets one CTA more than a tile has
 };
 
 cudaError_t prefill_init_attributes();

@@ -250,7 +250,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     if (pre) {
       // On a timeout (status bit set) every stage is still loaded and consumed, so no
       // copy is left in flight, and the epilogue writes nothing.
-      if (!wait_at_least(p.tile_done + blockIdx.y, p.tile_need, p.status, kDefaultWaitNs)) s_stale = 1;
+      if (!wait_at_least(p.tile_done + blockIdx.y, p.tile_need, p.status, p.wait_ns ? p.wait_ns : kDefaultWaitNs))
+        s_stale = 1;
       asm volatile("fence.proxy.async.global;" ::: "memory");  // h rows were written by generic stores
     }
     for (int kb = 0; kb < nk; ++kb) {
@@ -447,7 +448,8 @@ cudaError_t launch_tc_prefill(const TcPrefillArgs& a, cudaStream_t st) {
   const int max_tiles = (Tk + BM - 1) / BM + a.G;
   const int cb1 = a.I / (BN / 2), cb2 = a.H / BN;  // column blocks of the two GEMMs
   p.tile_done = a.tile_done;
-  p.tile_need = (uint32_t)cb1;
+  p.tile_need = (uint32_t)cb1 + (a.stall ? 1u : 0u);  // (stall: a target no tile reaches, so the wait runs out)
+  p.wait_ns = a.wait_ns;
   if (a.tile_done &&
       (e = cudaMemsetAsync(a.tile_done, 0, sizeof(uint32_t) * (size_t)max_tiles, st)) != cudaSuccess)
     return e;

@@ -20,6 +20,7 @@ struct TcGemmArgs {
   // rows once the count reaches tile_need. nullptr: the down launch follows gate/up.
   uint32_t* tile_done;
   uint32_t tile_need;
+  unsigned long long wait_ns;  // bound of the tile-count wait (0: kDefaultWaitNs)
 };
 
 struct TcPrefillArgs {
@@ -37,6 +38,8 @@ struct TcPrefillArgs {
   float* y;                // [Tk, H]
   uint32_t* status;
   uint32_t* tile_done;     // [ceil(Tk/128) + G] scratch, zeroed here each call; nullptr: no early down
+  unsigned long long wait_ns;  // bound of the down CTAs' tile-count wait (0: the 2 s default)
+  int stall;                   // debug: the tile-count target is one gate/up CTA above the tile's
   cudaEvent_t ev_gemm_begin;  // recorded before the gate/up launch (nullptr: none)
   cudaEvent_t ev_gemm_end;    // recorded after the down launch (nullptr: none)
 };

@@ -440,14 +440,17 @@ moe_status_t moe_offload_host_read_gbs(int device, const void* host_ptr, size_t 
 
 /* Bounded waits, for tests that make one run out (no counterpart on the pages).
  * In a decode step the down launch waits per expert group, on counters the
- * gate/up CTAs raise, for at most limit_ns (0 = the default, 2 s) per wait;
- * when a wait runs out the kernel sets MOE_DEV_TIMEOUT, computes on, and every
- * later wait of the handle returns at once until moe_offload_reset, so outputs
- * are invalid while the bit is set. stall = 1 makes the first group's wait of
- * every down warp target one gate/up CTA more than its column has: it runs out
- * after limit_ns on each later decode step; stall = 0 removes that. Host only;
- * applies to launches enqueued after the call (decode graphs keep the values
- * they were captured with). */
+ * gate/up CTAs raise, and in a prefill call the down GEMM's CTAs wait per row
+ * tile on counts the gate/up GEMM's CTAs raise, for at most limit_ns (0 = the
+ * default, 2 s) per wait; when a wait runs out the kernel sets MOE_DEV_TIMEOUT,
+ * computes on (a prefill down CTA whose wait ran out still loads and consumes
+ * every stage of its ring, so no copy is left in flight, and writes no output),
+ * and every later wait of the handle returns at once until moe_offload_reset, so
+ * outputs are invalid while the bit is set. stall = 1 makes the first group's
+ * wait of every decode down warp, and every prefill tile wait, target one
+ * gate/up CTA more than there is: it runs out after limit_ns on each later
+ * call; stall = 0 removes that. Host only; applies to launches enqueued after
+ * the call (decode graphs keep the values they were captured with). */
 moe_status_t moe_offload_debug_wait(moe_offload_t h, long long limit_ns, int stall);
 
 /* ---- Decode trace (observability; no counterpart on the pages) ---------

@@ -217,6 +217,56 @@ def test_bounded_early_down_wait_runs_out_and_reset_recovers(dev, tiny):
         h.close()
 
 
+def test_bounded_prefill_tile_wait_runs_out_and_reset_recovers(dev):
+    """The same, for the tensor-core prefill GEMMs: the down GEMM's CTAs start under
+    the gate/up GEMM and wait per row tile for its gate/up CTAs to count themselves
+    done. With a 1 ms bound and the debug stall (a target one CTA above what a tile
+    has) every such wait runs out: the call returns at once, the status word carries
+    MOE_DEV_TIMEOUT and nothing else (each down CTA still loaded and consumed its
+    whole ring, so no copy was left in flight), and after reset, with the stall
+    removed, a staged prefill computes the oracle's outputs again, row by row."""
+    import time
+    from expert_cache_router_gb300 import MoeOffloadError
+    from expert_cache_router_gb300._lib import MOE_DEV_TIMEOUT
+    from parity import check_layer
+    T = 48
+    st = Stack(TINY, num_layers=2, tokens=1, batch=T, stream=8)
+    c = st.cfg
+    h = st.handle(torch, dev, num_slots=4)     # 8 experts over 4 slots: every call stages
+    try:
+        xd = _bits(st.x[0, :, :T]).to(dev)
+        out = torch.empty((T, c.hidden), dtype=torch.int16, device=dev)
+        h.decode_layer(0, xd[0], T, out)          # warm: kernels loaded, scratch sized
+        torch.cuda.synchronize()
+        assert h.prefill_times()["staged"]
+        h.reset()
+        h.debug_wait(limit_ns=1_000_000, stall=True)
+        t0 = time.perf_counter()
+        h.decode_layer(0, xd[0], T, out)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+        assert elapsed < 0.5, elapsed
+        with pytest.raises(MoeOffloadError) as ei:
+            h.get_stats()
+        assert ei.value.status == MOE_ERR_DEVICE_STATUS
+        assert h.get_stats(check=False)["device_status"] == MOE_DEV_TIMEOUT
+        h.debug_wait(limit_ns=0, stall=False)
+        h.reset()
+        assert h.get_stats()["device_status"] == 0
+        for l in range(c.num_layers):
+            h.decode_layer(l, xd[l], T, out)
+            ids = torch.empty((T, c.top_k), dtype=torch.int32, device=dev)
+            w = torch.empty((T, c.top_k), dtype=torch.float32, device=dev)
+            h.route_topk(l, xd[l], T, ids, w)
+            torch.cuda.synchronize()
+            assert h.prefill_times()["staged"]
+            check_layer(out.cpu().numpy().view(np.uint16), st.x[0, l, :T], st.wr[l], st.w13[l], st.w2[l],
+                        c.top_k, c.renormalize, ids.cpu().numpy(), w.cpu().numpy(), ctx=l)
+        assert h.get_stats()["device_status"] == 0
+    finally:
+        h.close()
+
+
 def test_debug_wait_rejects_bad_arguments(dev, tiny):
     from expert_cache_router_gb300 import MoeOffloadError
     h = tiny.handle(torch, dev)
