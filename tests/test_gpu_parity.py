@@ -640,6 +640,32 @@ def test_prefill_full_size_qwen3_30b_a3b(dev):
                 gw[sample])
 
 
+def test_prefill_mixtral_8x7b_layer_full_size(dev):
+    """Tensor-core prefill on one Mixtral-8x7B-shaped layer (E=8, k=2, H=4096, I=14336,
+    S=4, 512 tokens, staged): 112 gate/up and 16 down column blocks per row tile, K up
+    to 14336; sampled rows, near-ties included, against the oracle on the GPU's routing."""
+    T = 512
+    st_ = Stack(MIXTRAL_8X7B, num_layers=1, tokens=1, batch=T, stream=9)
+    c = st_.cfg
+    h = st_.handle(torch, dev, num_slots=4)
+    try:
+        x = st_.x[0, 0, :T]
+        out = torch.empty((T, c.hidden), dtype=torch.int16, device=dev)
+        h.decode_layer(0, _bits(x).to(dev), T, out)
+        torch.cuda.synchronize()
+        times = h.prefill_times()
+        gemm_kernels = h.prefill_gemm_ms()
+        stats = h.get_stats()
+        gids, gw = _gpu_route(h, 0, x, dev)
+    finally:
+        h.close()
+    assert times["staged"] and stats["device_status"] == 0
+    assert 0 < gemm_kernels <= times["gemm"]
+    sample = np.arange(0, T, 29)
+    check_layer(_u16(out)[sample], x[sample], st_.wr[0], st_.w13[0], st_.w2[0], c.top_k, True, gids[sample],
+                gw[sample])
+
+
 @pytest.mark.parametrize("T, S, staged", [(333, 25, True), (64, 128, False)])
 def test_prefill_ragged_and_slot_path_qwen3_30b_a3b(dev, T, S, staged):
     """Tensor-core prefill on one full Qwen3-30B-A3B layer at a token count that leaves
