@@ -14,9 +14,11 @@
 //
 // Two CTAs per SM (256 TMEM columns and a 96 KB ring each), so that one CTA's
 // epilogue, which leaves the tensor core and the copies idle, overlaps the other
-// CTA's main loop. At prefill sizes (about 128 rows per expert) the kernels are
-// bound by the bytes they stream; the ring is made of small stages (K = 32,
-// 64-byte swizzle).
+// CTA's main loop. The ring holds two stages of K = 64 (128-byte swizzle): at
+// prefill sizes of the Qwen3-30B-A3B shape (about 128 rows per expert) the kernels
+// are bound by the bytes they stream and the stage size does not matter; at the
+// Mixtral-8x7B shape (I = 14336, tensor-bound) the larger stages halve the
+// per-stage barrier and commit work of the MMA thread.
 //
 // Early down: the down launch follows the gate/up launch under programmatic
 // dependent launch. Each gate/up CTA triggers it at its start and, once its h
@@ -28,7 +30,7 @@
 // producer off the GPU.
 //
 // Warp roles (8 warps): warp 0 allocates TMEM and, one lane, issues the TMA
-// loads of a 4-stage shared-memory ring (K = 32 each); warp 1, one lane, issues
+// loads of a 2-stage shared-memory ring (K = 64 each); warp 1, one lane, issues
 // tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate) and commits each
 // stage back to the producer; all 8 warps read the accumulator with tcgen05.ld
 // for the epilogue (warp w reads TMEM lanes 32(w%4)..32(w%4)+31 = tile rows and
@@ -49,10 +51,10 @@ namespace {
 
 constexpr int BM = 128;        // tile rows (pairs)
 constexpr int BN = 256;        // accumulator columns
-constexpr int BK = 32;         // K per stage: one 64-byte swizzle row of bf16
+constexpr int BK = 64;         // K per stage: one 128-byte swizzle row of bf16
 constexpr int A_BYTES = BM * BK * 2;     // 8 KB
 constexpr int B_BYTES = BN * BK * 2;     // 16 KB
-constexpr int kStages = 4;
+constexpr int kStages = 2;
 constexpr int kStageBytes = A_BYTES + B_BYTES;
 constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;  // ring, 1 KB alignment slack, barriers
 constexpr uint32_t kTmemCols = BN;
@@ -96,15 +98,16 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* tm, uint64_t* bar
       : "memory");
 }
 
-// Shared-memory matrix descriptor: K-major operand, 64-byte swizzle, 8-row
-// groups 512 bytes apart (the layout a SWIZZLE_64B TMA box of 32 bf16 columns writes).
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (the layout a SWIZZLE_128B TMA box of 64 bf16 columns writes).
+// The k-th K=16 step of a stage starts 32 bytes further into the swizzled rows.
 __device__ __forceinline__ uint64_t sdesc(const void* p) {
   const uint64_t a = smem_u32(p);
   uint64_t d = (a >> 4) & 0x3FFFull;        // start address
   d |= 1ull << 16;                          // leading byte offset (unused with this swizzle)
-  d |= (uint64_t)(512 >> 4) << 32;          // stride byte offset: 8 rows x 64 B
+  d |= (uint64_t)(1024 >> 4) << 32;         // stride byte offset: 8 rows x 128 B
   d |= 1ull << 46;                          // descriptor version
-  d |= 4ull << 61;                          // 64-byte swizzle
+  d |= 2ull << 61;                          // 128-byte swizzle
   return d;
 }
 
@@ -397,14 +400,14 @@ cudaError_t encoder() {
   return cudaSuccess;
 }
 
-// 2-D bf16 tensor map [rows, cols] (cols contiguous), box rows x 32 columns, 64-byte swizzle.
+// 2-D bf16 tensor map [rows, cols] (cols contiguous), box rows x 64 columns, 128-byte swizzle.
 cudaError_t make_map(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
