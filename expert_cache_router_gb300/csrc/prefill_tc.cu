@@ -166,26 +166,38 @@ __device__ __forceinline__ void store_rows(const uint32_t* tile, int lane, Dst d
   }
 }
 
-// Tile t -> (bucket, first row of the tile in bucket order, valid rows).
-__device__ bool tile_of(const int32_t* counts, const int32_t* offsets, const int32_t* tiles, int G, int t,
-                        int* g_out, int* row0, int* rows) {
+// The CTA's work: bucket g, row tile (global index), column block, first row in bucket
+// order and valid rows. CTAs run in launch order (linear id L), and bucket g owns the
+// cb x R_g consecutive ids from cb * tiles[g]; within them the R_g row tiles of one
+// column block are adjacent, so the CTAs that stream the same weight block run
+// together (it is read from DRAM once however many rows the bucket has), and a row
+// tile's x (or h) tile is read by CTAs at most R_g ids apart, also running together.
+__device__ bool cta_work(const int32_t* counts, const int32_t* offsets, const int32_t* tiles, int G, int cb,
+                         int* g_out, int* tile, int* col, int* row0, int* rows) {
+  const int L = blockIdx.x + gridDim.x * blockIdx.y;
+  const int t = L / cb;  // cb * tiles[g] <= L exactly when tiles[g] <= t
   if (t >= tiles[G]) return false;
   int lo = 0, hi = G - 1;
-  while (lo < hi) {  // largest g with tiles[g] <= t
+  while (lo < hi) {  // largest g with tiles[g] <= t (never an empty bucket: it shares the next one's offset)
     const int mid = (lo + hi + 1) >> 1;
     if (tiles[mid] <= t) lo = mid;
     else hi = mid - 1;
   }
-  const int m0 = (t - tiles[lo]) * BM;
+  const int R = tiles[lo + 1] - tiles[lo];
+  const int j = L - cb * tiles[lo];
+  const int c = j / R, r = j - c * R;
+  const int m0 = r * BM;
   *g_out = lo;
+  *tile = tiles[lo] + r;
+  *col = c;
   *row0 = offsets[lo] + m0;
   *rows = min(BM, counts[lo] - m0);
   return *rows > 0;
 }
 
-// MODE 1: gate/up + SiLU epilogue into Hp; column block j = blockIdx.x: gate rows
-// j*128.. and the matching up rows I + j*128.. in one accumulator (h columns
-// j*128..). MODE 2: down projection into Y by pair, output columns j*256...
+// MODE 1: gate/up + SiLU epilogue into Hp; column block j: gate rows j*128.. and the
+// matching up rows I + j*128.. in one accumulator (h columns j*128..). MODE 2: down
+// projection into Y by pair, output columns j*256...
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, kCtasPerSm)
 tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b, TcGemmArgs p) {
@@ -199,11 +211,8 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   __shared__ int s_stale;  // early down: the tile's h rows did not arrive in time (no output written)
 
   if (MODE == 1) pdl_trigger();  // the down launch may start once every gate/up CTA has started
-  // blockIdx.x: column block, blockIdx.y: row tile. The CTAs of one tile are adjacent in
-  // launch order, so they run together and its x (or h) tile is read from DRAM once and then
-  // from L2; so are the tiles of one bucket, which share its weights.
-  int g, row0, rows;
-  if (!tile_of(p.counts, p.offsets, p.tiles, p.G, blockIdx.y, &g, &row0, &rows)) return;
+  int g, tile, col, row0, rows;
+  if (!cta_work(p.counts, p.offsets, p.tiles, p.G, p.cb, &g, &tile, &col, &row0, &rows)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = p.K / BK;
 
@@ -236,11 +245,11 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     auto load_b = [&](int kb, uint8_t* a_dst, uint64_t* bar) {
       uint8_t* b_dst = a_dst + A_BYTES;
       if (MODE == 1) {
-        const int gate_row = g * 2 * p.I + blockIdx.x * (BN / 2);
+        const int gate_row = g * 2 * p.I + col * (BN / 2);
         tma_load_2d(tmb, bar, b_dst, kb * BK, gate_row);
         tma_load_2d(tmb, bar, b_dst + B_BYTES / 2, kb * BK, gate_row + p.I);
       } else {
-        tma_load_2d(tmb, bar, b_dst, kb * BK, g * p.H + blockIdx.x * BN);
+        tma_load_2d(tmb, bar, b_dst, kb * BK, g * p.H + col * BN);
       }
     };
     // Early down: the weight tiles of the first stages do not depend on the gate/up
@@ -253,7 +262,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     if (pre) {
       // On a timeout (status bit set) every stage is still loaded and consumed, so no
       // copy is left in flight, and the epilogue writes nothing.
-      if (!wait_at_least(p.tile_done + blockIdx.y, p.tile_need, p.status, p.wait_ns ? p.wait_ns : kDefaultWaitNs))
+      if (!wait_at_least(p.tile_done + tile, p.tile_need, p.status, p.wait_ns ? p.wait_ns : kDefaultWaitNs))
         s_stale = 1;
       asm volatile("fence.proxy.async.global;" ::: "memory");  // h rows were written by generic stores
     }
@@ -312,7 +321,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     if (MODE == 1) {
       constexpr int kPart = BN / 2 / kColParts;  // this warp's h columns (gate in 0..127, up in 128..255)
       static_assert(kPart == 64, "epilogue column split");
-      const int col0 = blockIdx.x * (BN / 2) + part * kPart;
+      const int col0 = col * (BN / 2) + part * kPart;
 #pragma unroll 1
       for (int c = 0; c < kPart; c += 32) {
         uint32_t gv[32], uv[32];
@@ -337,7 +346,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
         return row < rows ? reinterpret_cast<uint32_t*>(p.hp + (size_t)(row0 + row) * p.I + col0) : nullptr;
       });
     } else {
-      const int col0 = blockIdx.x * BN;
+      const int col0 = col * BN;
       const int pair = r < rows ? p.perm[row0 + r] : 0;
       constexpr int kPart = BN / kColParts;
       static_assert(kPart % 32 == 0, "epilogue column split");
@@ -365,7 +374,7 @@ tc_grouped_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   __syncthreads();
   if (MODE == 1 && p.tile_done && threadIdx.x == 0) {  // early down: this CTA's h rows are written
     __threadfence();
-    atomicAdd(p.tile_done + blockIdx.y, 1u);
+    atomicAdd(p.tile_done + tile, 1u);
   }
   if (warp == 0) {
     tc_fence_after();
@@ -457,10 +466,12 @@ cudaError_t launch_tc_prefill(const TcPrefillArgs& a, cudaStream_t st) {
       (e = cudaMemsetAsync(a.tile_done, 0, sizeof(uint32_t) * (size_t)max_tiles, st)) != cudaSuccess)
     return e;
   p.K = a.H;
+  p.cb = cb1;
   if (a.ev_gemm_begin && (e = cudaEventRecord(a.ev_gemm_begin, st)) != cudaSuccess) return e;
   tc_grouped_gemm<1><<<dim3(cb1, max_tiles), kGemmThreads, kSmemBytes, st>>>(ta1, tb1, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   p.K = a.I;
+  p.cb = cb2;
   if ((e = launch_k(tc_grouped_gemm<2>, dim3(cb2, max_tiles), dim3(kGemmThreads), kSmemBytes, st,
                     a.tile_done != nullptr, ta2, tb2, p)) != cudaSuccess)
     return e;

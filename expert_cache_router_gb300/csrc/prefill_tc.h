@@ -11,6 +11,7 @@ struct TcGemmArgs {
   const int32_t* offsets;  // first row of each bucket [G+1]
   const int32_t* tiles;    // first 128-row tile of each bucket [G+1]
   int G, K, I, H;
+  int cb;                  // column blocks of this GEMM (grid x)
   const int32_t* perm;     // bucket-order row -> pair
   uint16_t* hp;            // [Tk, I] bf16 (gate/up output)
   float* y;                // [Tk, H] fp32, by pair (down output)
